@@ -1,0 +1,238 @@
+"""Float64 CPU oracle for the memory-efficient ("linear") GRPO loss.
+
+TEST INFRASTRUCTURE ONLY. Only the test suite, the smoke check and the CPU
+baseline leg of the benchmark may import this module. The product path (the
+CUDA library and its Python binding) never calls it and shares no code with
+it: there is no CPU fallback.
+
+What it computes is the plain definition the fused method reaches (up to
+rounding order), written out with the full [rows, vocab] logits
+materialised in float64:
+
+* Group-relative advantages. The "Group Relative" part of GRPO samples
+  several answers per prompt, scores them, and derives an advantage from the
+  rewards statistically instead of from a value model (aibit.im GRPO blog,
+  section on GRPO; zjt100.com translation of the Unsloth GRPO blog, "GRPO
+  的数学和发现的问题", where A is the advantage after all reward functions).
+  The pages print no formula; the reading used here is
+  A_b = (r_b - mean_g r) / (std_g r + eps) over each group of G contiguous
+  sequences, with Bessel's correction unless ``std_unbiased`` is 0.
+* Token log-probabilities from the lm_head projection in float64 with the
+  logsumexp trick (same page, closing remark of "GRPO 的数学和发现的问题";
+  Unsloth "grpo-long-context" page, flattened sequence chunking, where the
+  chunked logits are upcast to float32 and the selected token's log-softmax
+  is gathered). Row n of H scores token ids[n].
+* The per-token objective exp(q - q.detach()) * A - beta * KL with the
+  reverse-KL estimator KL = exp(p - q) - (p - q) - 1, beta = 0.04, q the
+  policy log-prob and p the frozen reference log-prob (zjt100.com page,
+  "GRPO 的数学和发现的问题": reverse KL, beta 0.04, Q the trained model and P
+  the reference; Schulman's unbiased estimator needs no extra Q factor; the
+  exp(q - q.detach()) factor has value 1 and must stay). The loss is the
+  negative objective, a masked mean over each sequence's tokens followed by
+  a mean over the B sequences.
+* The backward pass as the closed-form derivative of that loss. The detach
+  makes the advantage term contribute A * dq. With x = p - q the derivative
+  of the per-token loss with respect to q is -(A + beta * (exp(x) - 1)), and
+  dq/dz = onehot(y) - softmax(z). The recompute-in-backward of the Unsloth
+  "grpo-long-context" page (offloaded log-softmax section) changes where the
+  logits come from, not this value.
+
+All inputs are taken at their exact values (bf16 and float32 upcast exactly to
+float64). Functions that take ``rows`` compute the listed rows only; every
+per-row quantity depends on that row alone, apart from the per-sequence
+token counts, which always come from the whole mask.
+"""
+from __future__ import annotations
+
+from typing import Dict, Optional, Sequence
+
+import numpy as np
+
+__all__ = [
+    "to_f64", "advantages", "sequence_weights", "token_logprobs", "kl_estimator",
+    "forward", "loss_coefficients", "backward", "logit_memory_gib",
+    "hidden_state_memory_gib",
+]
+
+
+def to_f64(x) -> np.ndarray:
+    """Exact float64 copy of a numpy array or a (CPU) torch tensor of any
+    float dtype, bf16 included."""
+    if hasattr(x, "detach"):  # torch tensor
+        t = x.detach().cpu()
+        if t.is_floating_point():
+            t = t.double()
+        return t.numpy()
+    return np.asarray(x, dtype=np.float64)
+
+
+def advantages(rewards, group_size: int, eps: float, std_unbiased: int = 1) -> np.ndarray:
+    """Group-relative advantages, float64 [B].
+
+    Each group is G contiguous entries of ``rewards``. The mean is taken over
+    the group, the standard deviation with ddof 1 (``std_unbiased``) or 0,
+    and A = (r - mean) / (std + eps).
+    """
+    r = to_f64(rewards).reshape(-1)
+    B, G = r.shape[0], int(group_size)
+    if G < 1 or B % G != 0:
+        raise ValueError("group_size must divide the number of sequences")
+    ddof = 1 if std_unbiased else 0
+    if G - ddof < 1:
+        raise ValueError("an unbiased std needs at least two members per group")
+    g = r.reshape(B // G, G)
+    mean = g.sum(axis=1, keepdims=True) / G
+    var = ((g - mean) ** 2).sum(axis=1, keepdims=True) / (G - ddof)
+    return ((g - mean) / (np.sqrt(var) + eps)).reshape(B)
+
+
+def sequence_weights(mask, num_seqs: int, seq_len: int):
+    """Per-token weights w_n = m_n / (B * max(cnt_b, 1)) and counts cnt_b.
+
+    A sequence with no valid token contributes nothing but still counts in B.
+    """
+    m = to_f64(mask).reshape(num_seqs, seq_len)
+    cnt = m.sum(axis=1)
+    w = m / (num_seqs * np.maximum(cnt, 1.0))[:, None]
+    return w.reshape(-1), cnt
+
+
+def token_logprobs(H, W, ids, rows: Optional[Sequence[int]] = None, row_block: int = 256):
+    """log softmax(H W^T)[n, ids[n]] and the row logsumexp, float64.
+
+    The full vocab row of logits is formed for every row (in blocks of
+    ``row_block`` rows to bound memory); lse = max + log(sum(exp(z - max))).
+    Returns (logp [R], lse [R]) for the requested rows (all rows by default).
+    """
+    Hs = H if rows is None else H[np.asarray(rows)]
+    Hf = to_f64(Hs)
+    Wf = to_f64(W)
+    ids_all = np.asarray(to_f64(ids), dtype=np.int64).reshape(-1)
+    sel = ids_all if rows is None else ids_all[np.asarray(rows)]
+    V = Wf.shape[0]
+    if sel.size and (sel.min() < 0 or sel.max() >= V):
+        raise ValueError("token id out of range")
+    R = Hf.shape[0]
+    logp = np.empty(R)
+    lse = np.empty(R)
+    for r0 in range(0, R, row_block):
+        r1 = min(R, r0 + row_block)
+        Z = Hf[r0:r1] @ Wf.T
+        zmax = Z.max(axis=1)
+        s = np.exp(Z - zmax[:, None]).sum(axis=1)
+        lse[r0:r1] = zmax + np.log(s)
+        logp[r0:r1] = Z[np.arange(r1 - r0), sel[r0:r1]] - lse[r0:r1]
+    return logp, lse
+
+
+def kl_estimator(logp_pol, logp_ref) -> np.ndarray:
+    """Reverse-KL estimator exp(x) - x - 1 with x = p - q, evaluated as
+    expm1(x) - x (the same number, without cancellation for small x)."""
+    x = np.asarray(logp_ref, np.float64) - np.asarray(logp_pol, np.float64)
+    return np.expm1(x) - x
+
+
+def forward(H_pol, H_ref, W, ids, mask, adv, num_seqs: int, seq_len: int,
+            beta: float) -> Dict[str, np.ndarray]:
+    """The GRPO loss forward pass over all N = num_seqs * seq_len tokens.
+
+    Returns logp_pol, logp_ref, lse_pol (per token; log-probs are 0 at
+    masked tokens), kl (0 at masked tokens), weights w, loss and kl_mean
+    (masked mean of KL; 0 when no token is valid).
+    """
+    m = to_f64(mask).reshape(-1)
+    A = to_f64(adv).reshape(-1)
+    # masked tokens may carry any id (e.g. a padding label); score id 0 there
+    ids_safe = np.where(m > 0, np.asarray(to_f64(ids), dtype=np.int64).reshape(-1), 0)
+    Wf = to_f64(W)
+    q, lse_q = token_logprobs(H_pol, Wf, ids_safe)
+    p, _ = token_logprobs(H_ref, Wf, ids_safe)
+    q = np.where(m > 0, q, 0.0)
+    p = np.where(m > 0, p, 0.0)
+    kl = np.where(m > 0, kl_estimator(q, p), 0.0)
+    w, cnt = sequence_weights(m, num_seqs, seq_len)
+    A_tok = np.repeat(A, seq_len)
+    # exp(q - q.detach()) has value 1, so the per-token loss is -(A - beta KL)
+    ell = -(A_tok - beta * kl)
+    loss = float(np.sum(w * ell))
+    nvalid = m.sum()
+    kl_mean = float(np.sum(m * kl) / nvalid) if nvalid > 0 else 0.0
+    return {"logp_pol": q, "logp_ref": p, "lse_pol": lse_q, "kl": kl, "w": w,
+            "cnt": cnt, "loss": loss, "kl_mean": kl_mean}
+
+
+def loss_coefficients(logp_pol, logp_ref, adv_tok, w, beta: float, grad_loss: float) -> np.ndarray:
+    """c_n = -dLoss/dq_n = g * w_n * (A_b + beta * (exp(x_n) - 1)), x = p - q.
+
+    Derivation: the per-token loss is -(A exp(q - sg(q)) - beta KL(x)); its
+    q-derivative is -A + beta dKL/dq with dKL/dq = 1 - exp(x).
+    """
+    x = np.asarray(logp_ref, np.float64) - np.asarray(logp_pol, np.float64)
+    return grad_loss * np.asarray(w, np.float64) * (np.asarray(adv_tok, np.float64) + beta * np.expm1(x))
+
+
+def backward(H_pol, H_ref, W, ids, mask, adv, num_seqs: int, seq_len: int, beta: float,
+             grad_loss: float = 1.0, rows: Optional[Sequence[int]] = None,
+             want_dW: bool = False, want_dZ: bool = False, row_block: int = 256):
+    """Gradients of the loss: dH_pol (rows requested, or all) and optionally dW.
+
+    Per row: q and p from ``token_logprobs`` (the reference rows are needed
+    for x = p - q), c_n from ``loss_coefficients``, then
+    dZ_n = c_n * (softmax(z_n) - onehot(ids_n)), dH_n = dZ_n W and
+    dW = sum_n dZ_n^T H_pol[n]. Masked rows have c = 0.
+    ``want_dW`` requires all rows.
+    """
+    m = to_f64(mask).reshape(-1)
+    A = to_f64(adv).reshape(-1)
+    N = m.shape[0]
+    rows_arr = np.arange(N) if rows is None else np.asarray(rows, dtype=np.int64)
+    if want_dW and rows is not None:
+        raise ValueError("dW needs every row")
+    w, _ = sequence_weights(m, num_seqs, seq_len)
+    Wf = to_f64(W)
+    V, d = Wf.shape
+    ids_all = np.asarray(to_f64(ids), dtype=np.int64).reshape(-1)
+    dH = np.zeros((rows_arr.size, d))
+    dW = np.zeros((V, d)) if want_dW else None
+    dZ_all = np.zeros((rows_arr.size, V)) if want_dZ else None
+    for r0 in range(0, rows_arr.size, row_block):
+        rr = rows_arr[r0:r0 + row_block]
+        valid = m[rr] > 0
+        Hp = to_f64(H_pol[rr])
+        Z = Hp @ Wf.T
+        zmax = Z.max(axis=1)
+        lse = zmax + np.log(np.exp(Z - zmax[:, None]).sum(axis=1))
+        sel = ids_all[rr]
+        safe = np.where(valid, sel, 0)
+        q = Z[np.arange(rr.size), safe] - lse
+        p, _ = token_logprobs(H_ref, Wf, ids_all, rows=rr[valid]) if valid.any() else (np.zeros(0), None)
+        p_full = np.zeros(rr.size)
+        p_full[valid] = p
+        c = loss_coefficients(q, p_full, A[rr // seq_len], w[rr], beta, grad_loss)
+        c = np.where(valid, c, 0.0)
+        dZ = np.exp(Z - lse[:, None])
+        dZ[np.arange(rr.size), safe] -= 1.0
+        dZ *= c[:, None]
+        dH[r0:r0 + rr.size] = dZ @ Wf
+        if want_dW:
+            dW += dZ.T @ Hp
+        if want_dZ:
+            dZ_all[r0:r0 + rr.size] = dZ
+    out = {"dH": dH, "rows": rows_arr}
+    if want_dW:
+        out["dW"] = dW
+    if want_dZ:
+        out["dZ"] = dZ_all
+    return out
+
+
+def logit_memory_gib(rows: int, vocab: int, multiplier: int = 1, bytes_per_elem: int = 1) -> float:
+    """Logits footprint of the Unsloth long-context page's memory model:
+    rows * vocab / multiplier elements, over 1024^3 (Equations 1 to 3 count
+    elements; pass bytes_per_elem=4 for float32 bytes)."""
+    return rows / multiplier * vocab * bytes_per_elem / 1024 ** 3
+
+
+def hidden_state_memory_gib(batch: int, context: int, hidden: int) -> float:
+    """Hidden-state footprint of the same page: batch * context * hidden / 1024^3."""
+    return batch * context * hidden / 1024 ** 3

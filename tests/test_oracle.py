@@ -1,0 +1,252 @@
+"""Pins of the float64 oracle against facts fixed outside the oracle itself:
+hand-worked closed forms, library routines on special cases, invariants the
+pages state, a literal autograd of the objective, finite differences, and
+the pages' printed memory figures. CPU only."""
+import os
+
+import numpy as np
+import pytest
+import scipy.special
+import torch
+
+from oracle import grpo_oracle as O
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# ----------------------------------------------------------------- advantages
+
+def test_advantages_hand_worked_group():
+    # rewards 0,1,2,3: mean 1.5; squared deviations 2.25+0.25+0.25+2.25 = 5
+    A = O.advantages([0.0, 1.0, 2.0, 3.0], 4, eps=1e-4, std_unbiased=1)
+    std = np.sqrt(5.0 / 3.0)            # ddof 1: 5 / 3
+    assert np.allclose(A, np.array([-1.5, -0.5, 0.5, 1.5]) / (std + 1e-4), rtol=1e-15)
+    A0 = O.advantages([0.0, 1.0, 2.0, 3.0], 4, eps=1e-4, std_unbiased=0)
+    assert np.allclose(A0, np.array([-1.5, -0.5, 0.5, 1.5]) / (np.sqrt(1.25) + 1e-4), rtol=1e-15)
+
+
+def test_advantages_pair_and_constant_groups():
+    # group {0, 2}: mean 1, ddof-1 std sqrt(2); group {5, 5}: all equal -> 0
+    A = O.advantages([0.0, 2.0], 2, eps=0.0, std_unbiased=1)
+    s = 1.0 / np.sqrt(2.0)
+    assert np.allclose(A, [-s, s], rtol=1e-15, atol=0)
+    assert np.all(O.advantages([5.0, 5.0, 0.0, 2.0], 2, eps=1e-4, std_unbiased=1)[:2] == 0.0)
+
+
+def test_advantages_match_torch_std_and_sum_to_zero():
+    g = torch.Generator().manual_seed(3)
+    r = torch.randn(12, 8, generator=g, dtype=torch.float64)
+    for unbiased in (True, False):
+        ref = (r - r.mean(1, keepdim=True)) / (r.std(1, keepdim=True, unbiased=unbiased) + 1e-4)
+        A = O.advantages(r.reshape(-1), 8, eps=1e-4, std_unbiased=int(unbiased))
+        assert np.allclose(A, ref.reshape(-1).numpy(), rtol=1e-13, atol=1e-14)
+        assert np.all(np.abs(A.reshape(12, 8).sum(1)) < 1e-12)
+
+
+def test_advantages_reject_bad_groups():
+    with pytest.raises(ValueError):
+        O.advantages([1.0, 2.0, 3.0], 2, 1e-4, 1)
+    with pytest.raises(ValueError):
+        O.advantages([1.0, 2.0], 1, 1e-4, 1)
+    assert np.all(O.advantages([1.0, 2.0], 1, 1e-4, 0) == 0.0)
+
+
+# ------------------------------------------------------------------ log-probs
+
+def _rand(shape, seed, scale=1.0):
+    g = torch.Generator().manual_seed(seed)
+    return scale * torch.randn(*shape, generator=g, dtype=torch.float64)
+
+
+def test_logprobs_match_torch_log_softmax_and_scipy_logsumexp():
+    H, W = _rand((300, 24), 1), _rand((700, 24), 2, 0.5)
+    ids = torch.randint(0, 700, (300,), generator=torch.Generator().manual_seed(4))
+    logp, lse = O.token_logprobs(H, W, ids, row_block=64)
+    Z = H @ W.T
+    ref = torch.log_softmax(Z, dim=1)[torch.arange(300), ids]
+    assert np.allclose(logp, ref.numpy(), rtol=1e-13, atol=1e-12)
+    assert np.allclose(lse, scipy.special.logsumexp(Z.numpy(), axis=1), rtol=1e-14)
+    # |z| < 30: the naive log(sum(exp(z))) is exact enough to compare against
+    assert float(Z.abs().max()) < 30
+    assert np.allclose(lse, np.log(np.exp(Z.numpy()).sum(1)), rtol=1e-13)
+
+
+def test_softmax_of_logprobs_sums_to_one():
+    H, W = _rand((1, 16), 5), _rand((257, 16), 6)
+    V = 257
+    logp, _ = O.token_logprobs(H.repeat(V, 1), W, np.arange(V))  # one row, every id
+    assert abs(np.exp(logp).sum() - 1.0) < 1e-13
+
+
+def test_logprobs_equal_logits_closed_form():
+    # every vocab row identical -> all logits equal to c = h.w -> lse = c + log V
+    V, d = 1000, 4
+    W = np.tile(np.array([[300.0, -2.0, 1.0, 0.5]]), (V, 1))
+    H = np.array([[4.0, 1.0, 0.0, 2.0]])
+    c = 4 * 300.0 - 2.0 + 0 + 1.0
+    logp, lse = O.token_logprobs(H, W, [17])
+    assert abs(lse[0] - (c + np.log(V))) < 1e-10
+    assert abs(logp[0] + np.log(V)) < 1e-12
+
+
+# ------------------------------------------------------------------------- KL
+
+def test_kl_estimator_properties():
+    x = np.array([-3.0, -1e-3, 0.0, 1e-6, 0.07, 2.0])
+    kl = O.kl_estimator(np.zeros_like(x), x)       # p - q = x
+    literal = np.exp(x) - x - 1.0
+    assert kl[2] == 0.0
+    assert np.all(kl >= 0)
+    # moderate x: equals the literal exp(x) - x - 1
+    assert np.allclose(kl[[0, 4, 5]], literal[[0, 4, 5]], rtol=1e-12)
+    # small x: the series x^2/2 + x^3/6 + x^4/24
+    s = x[[1, 3]]
+    assert np.allclose(kl[[1, 3]], s ** 2 / 2 + s ** 3 / 6 + s ** 4 / 24, rtol=1e-9)
+
+
+# --------------------------------------------------------------- small problem
+
+def _problem(B=8, T=6, G=4, d=12, V=40, seed=11, scale=0.4, ref_noise=0.3):
+    g = torch.Generator().manual_seed(seed)
+    N = B * T
+    Hp = torch.randn(N, d, generator=g, dtype=torch.float64)
+    Hr = Hp + ref_noise * torch.randn(N, d, generator=g, dtype=torch.float64)
+    W = scale * torch.randn(V, d, generator=g, dtype=torch.float64)
+    ids = torch.randint(0, V, (N,), generator=g)
+    mask = torch.ones(B, T, dtype=torch.uint8)
+    mask[1, T // 2:] = 0
+    mask[3, 1:] = 0
+    mask[B - 2, :] = 0                  # a sequence with no valid token
+    mask = mask.reshape(-1)
+    rewards = torch.randn(B, generator=g, dtype=torch.float64)
+    A = O.advantages(rewards, G, 1e-4, 1)
+    return dict(Hp=Hp, Hr=Hr, W=W, ids=ids, mask=mask, A=A, B=B, T=T, beta=0.04)
+
+
+def test_loss_at_reference_equal_policy_is_minus_mean_advantage():
+    P = _problem()
+    f = O.forward(P["Hp"], P["Hp"], P["W"], P["ids"], P["mask"], P["A"], P["B"], P["T"], P["beta"])
+    cnt = P["mask"].reshape(P["B"], P["T"]).sum(1).numpy()
+    expected = -np.sum(P["A"][cnt > 0]) / P["B"]
+    assert np.all(f["kl"] == 0.0) and f["kl_mean"] == 0.0
+    assert abs(f["loss"] - expected) < 1e-15
+    # and the KL part of the gradient vanishes: with A = 0 the gradient is 0
+    b = O.backward(P["Hp"], P["Hp"], P["W"], P["ids"], P["mask"], np.zeros(P["B"]), P["B"], P["T"],
+                   P["beta"], want_dW=True)
+    assert np.abs(b["dH"]).max() < 1e-15 and np.abs(b["dW"]).max() < 1e-15
+
+
+def test_beta_zero_loss_and_gradient_reduce_to_weighted_cross_entropy():
+    P = _problem()
+    f = O.forward(P["Hp"], P["Hr"], P["W"], P["ids"], P["mask"], P["A"], P["B"], P["T"], 0.0)
+    cnt = P["mask"].reshape(P["B"], P["T"]).sum(1).numpy()
+    assert abs(f["loss"] + np.sum(P["A"][cnt > 0]) / P["B"]) < 1e-15
+    # gradient = grad of sum_n w_n A_b CE(z_n, y_n) (library cross entropy)
+    H = P["Hp"].clone().requires_grad_(True)
+    W = P["W"].clone().requires_grad_(True)
+    ce = torch.nn.functional.cross_entropy(H @ W.T, P["ids"], reduction="none")
+    w = torch.from_numpy(O.sequence_weights(P["mask"], P["B"], P["T"])[0])
+    At = torch.from_numpy(np.repeat(P["A"], P["T"]))
+    (w * At * ce).sum().backward()
+    b = O.backward(P["Hp"], P["Hr"], P["W"], P["ids"], P["mask"], P["A"], P["B"], P["T"], 0.0,
+                   want_dW=True)
+    assert np.allclose(b["dH"], H.grad.numpy(), rtol=1e-11, atol=1e-15)
+    assert np.allclose(b["dW"], W.grad.numpy(), rtol=1e-11, atol=1e-15)
+
+
+def _literal_torch_loss(P, H, W, grad_scale=1.0):
+    """The objective written as the pages state it, under torch autograd:
+    exp(q - q.detach()) * A - beta * (exp(p - q) - (p - q) - 1), p from the
+    frozen reference (no gradient), masked mean per sequence, mean over B."""
+    B, T = P["B"], P["T"]
+    q = torch.log_softmax(H @ W.T, dim=1)[torch.arange(B * T), P["ids"]]
+    with torch.no_grad():
+        p = torch.log_softmax(P["Hr"] @ W.detach().T, dim=1)[torch.arange(B * T), P["ids"]]
+    A = torch.from_numpy(np.repeat(P["A"], T))
+    m = P["mask"].double()
+    obj = torch.exp(q - q.detach()) * A - P["beta"] * (torch.exp(p - q) - (p - q) - 1)
+    per_seq = (obj * m).reshape(B, T).sum(1) / m.reshape(B, T).sum(1).clamp(min=1)
+    return -grad_scale * per_seq.mean()
+
+
+def test_literal_autograd_matches_closed_form_forward_and_backward():
+    P = _problem()
+    H = P["Hp"].clone().requires_grad_(True)
+    W = P["W"].clone().requires_grad_(True)
+    L = _literal_torch_loss(P, H, W)
+    L.backward()
+    f = O.forward(P["Hp"], P["Hr"], P["W"], P["ids"], P["mask"], P["A"], P["B"], P["T"], P["beta"])
+    assert abs(f["loss"] - L.item()) < 1e-14
+    for g in (1.0, -2.5):
+        b = O.backward(P["Hp"], P["Hr"], P["W"], P["ids"], P["mask"], P["A"], P["B"], P["T"],
+                       P["beta"], grad_loss=g, want_dW=True)
+        assert np.allclose(b["dH"], g * H.grad.numpy(), rtol=1e-10, atol=1e-16)
+        assert np.allclose(b["dW"], g * W.grad.numpy(), rtol=1e-10, atol=1e-16)
+
+
+def test_finite_differences_of_surrogate():
+    """exp(q - sg(q)) has value 1 for every H, so the reported loss cannot be
+    differentiated numerically; the surrogate sum_n w_n (-A_b q_n + beta KL_n)
+    has the same gradient and can."""
+    P = _problem(B=4, T=4, G=2, d=8, V=32, seed=21, scale=0.8)
+    w, _ = O.sequence_weights(P["mask"], P["B"], P["T"])
+    At = np.repeat(P["A"], P["T"])
+    m = P["mask"].numpy() > 0
+    Hp, Hr, W = P["Hp"].numpy(), P["Hr"].numpy(), P["W"].numpy()
+    ids = P["ids"].numpy()
+
+    def Ls(Hp_, Wp_):
+        q, _ = O.token_logprobs(Hp_, Wp_, ids)
+        p, _ = O.token_logprobs(Hr, W, ids)          # frozen reference lm_head
+        kl = O.kl_estimator(q, p)
+        return float(np.sum(np.where(m, w * (-At * q + P["beta"] * kl), 0.0)))
+
+    b = O.backward(Hp, Hr, W, ids, P["mask"], P["A"], P["B"], P["T"], P["beta"], want_dW=True)
+    h = 1e-6
+    rng = np.random.default_rng(0)
+    for (i, j) in [tuple(rng.integers(0, s) for s in Hp.shape) for _ in range(12)]:
+        Hplus, Hminus = Hp.copy(), Hp.copy()
+        Hplus[i, j] += h
+        Hminus[i, j] -= h
+        fd = (Ls(Hplus, W) - Ls(Hminus, W)) / (2 * h)
+        assert abs(fd - b["dH"][i, j]) <= 1e-7 * max(1.0, abs(b["dH"][i, j])) + 1e-9
+    for (i, j) in [tuple(rng.integers(0, s) for s in W.shape) for _ in range(12)]:
+        Wplus, Wminus = W.copy(), W.copy()
+        Wplus[i, j] += h
+        Wminus[i, j] -= h
+        fd = (Ls(Hp, Wplus) - Ls(Hp, Wminus)) / (2 * h)
+        assert abs(fd - b["dW"][i, j]) <= 1e-7 * max(1.0, abs(b["dW"][i, j])) + 1e-9
+
+
+def test_row_structure_and_row_subsets():
+    P = _problem()
+    b = O.backward(P["Hp"], P["Hr"], P["W"], P["ids"], P["mask"], P["A"], P["B"], P["T"],
+                   P["beta"], want_dZ=True)
+    assert np.all(np.abs(b["dZ"].sum(1)) < 1e-15)              # softmax - onehot sums to 0
+    masked = P["mask"].numpy() == 0
+    assert np.all(b["dZ"][masked] == 0) and np.all(b["dH"][masked] == 0)
+    rows = np.array([0, 5, 9, 10, 33, 47])
+    bs = O.backward(P["Hp"], P["Hr"], P["W"], P["ids"], P["mask"], P["A"], P["B"], P["T"],
+                    P["beta"], rows=rows, row_block=4)
+    assert np.array_equal(bs["dH"], b["dH"][rows]) or np.allclose(bs["dH"], b["dH"][rows], rtol=1e-14, atol=1e-18)
+
+
+def test_masked_rows_may_carry_out_of_range_ids():
+    P = _problem()
+    ids = P["ids"].clone()
+    ids[P["mask"] == 0] = -100                  # a typical ignore label
+    f = O.forward(P["Hp"], P["Hr"], P["W"], ids, P["mask"], P["A"], P["B"], P["T"], P["beta"])
+    f0 = O.forward(P["Hp"], P["Hr"], P["W"], P["ids"], P["mask"], P["A"], P["B"], P["T"], P["beta"])
+    assert f["loss"] == f0["loss"]
+
+
+# -------------------------------------------------------------- memory model
+
+def test_memory_model_against_printed_figures():
+    with open(os.path.join(GOLDEN, "memory_figures.txt")) as fh:
+        rows = [l.split("|") for l in fh if l.strip() and not l.startswith("#")]
+    assert len(rows) == 4
+    for name, r, v, mult, bpe, printed, tol, _cite in rows:
+        val = O.logit_memory_gib(int(r), int(v), int(mult), int(bpe))
+        assert abs(val - float(printed)) <= float(tol), (name.strip(), val, printed)
+    assert abs(O.hidden_state_memory_gib(8, 64000, 4096) - 1.953125) < 1e-12
