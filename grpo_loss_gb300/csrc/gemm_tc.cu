@@ -1,0 +1,447 @@
+// Persistent tcgen05 GEMM with three fused epilogues:
+//
+//   MODE_FWD  Z = H W^T for policy and reference rows. Per row, an online
+//             max / sum-exp over the vocab tiles of one vocab slice (log2
+//             domain) and the gather of the target logit. The logits never
+//             leave tensor memory.
+//   MODE_DZ   Z = H_pol W^T recomputed for one chunk of rows; the epilogue
+//             writes dZ = c * (softmax(z) - onehot(y)) as bf16.
+//   MODE_DH   dH = dZ W for the same chunk (K = V), stored in H's dtype.
+//
+// One CTA per SM, 6 warps: warp 0 issues TMA loads into a 4-stage shared
+// memory ring, warp 1 owns tensor memory and issues the MMAs, warps 2..5 run
+// the epilogue, each thread owning one accumulator row (one TMEM lane).
+// Two 256-column accumulators in tensor memory let the epilogue of one tile
+// overlap the MMAs of the next.
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace grpo {
+
+namespace {
+
+constexpr int kStages = 4;
+constexpr int kBNMax = 256;
+constexpr int kAStageBytes = kBM * kBK * 2;     // 16 KB
+constexpr int kBStageBytes = kBNMax * kBK * 2;  // 32 KB
+constexpr int kThreads = 192;
+constexpr int kEpiThreads = 128;
+constexpr uint32_t kTmemCols = 512;
+constexpr int kAccStride = 256;  // TMEM columns per accumulator buffer
+constexpr int kSmemBytes =
+    1024 + kStages * (kAStageBytes + kBStageBytes) + 256;  // alignment slack + ring + barriers
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kGroupBlocks = 16;  // MODE_DZ raster: blocks per group sharing W tiles
+
+struct Smem {
+  uint64_t full[kStages];
+  uint64_t empty[kStages];
+  uint64_t acc_full[2];
+  uint64_t acc_empty[2];
+  uint64_t mma_done;
+  uint32_t tmem_base;
+  int abort;
+};
+
+// One unit of work: a run of output tiles sharing an A row block.
+struct Unit {
+  int side;      // MODE_FWD: 0 policy, 1 reference
+  int jj;        // block index (MODE_FWD: into blk; MODE_DZ/DH: within the chunk)
+  int a_row;     // first A row for TMA
+  int t0, t1;    // tile range [t0, t1) along N
+  int vs;        // MODE_FWD: vocab slice
+  int row0;      // first original row of the block (output rows)
+};
+
+template <int MODE>
+__device__ __forceinline__ int unit_count(const GemmArgs& g, int nb) {
+  if (MODE == MODE_FWD) return 2 * nb * g.n_vs;
+  const int nbc = min(g.chunk_nb, nb - g.chunk_b0);
+  if (nbc <= 0) return 0;
+  return MODE == MODE_DZ ? nbc * g.n_vt : nbc * g.n_nt;
+}
+
+template <int MODE>
+__device__ __forceinline__ Unit unit_decode(const GemmArgs& g, int nb, int u) {
+  Unit r;
+  if (MODE == MODE_FWD) {
+    const int i = u / g.n_vs;
+    r.vs = u - i * g.n_vs;
+    r.side = i >= nb ? 1 : 0;
+    r.jj = i - r.side * nb;
+    r.row0 = g.blk[r.jj] * kBM;
+    r.a_row = r.row0;
+    r.t0 = static_cast<int>((static_cast<int64_t>(r.vs) * g.n_vt) / g.n_vs);
+    r.t1 = static_cast<int>((static_cast<int64_t>(r.vs + 1) * g.n_vt) / g.n_vs);
+  } else if (MODE == MODE_DZ) {
+    const int nbc = min(g.chunk_nb, nb - g.chunk_b0);
+    const int gsz_full = kGroupBlocks * g.n_vt;
+    const int grp = u / gsz_full;
+    const int gb = min(kGroupBlocks, nbc - grp * kGroupBlocks);
+    const int rem = u - grp * gsz_full;
+    r.jj = grp * kGroupBlocks + rem % gb;
+    r.t0 = rem / gb;
+    r.t1 = r.t0 + 1;
+    r.side = 0;
+    r.vs = 0;
+    r.row0 = g.blk[g.chunk_b0 + r.jj] * kBM;
+    r.a_row = r.row0;
+  } else {
+    r.jj = u / g.n_nt;
+    r.t0 = u - r.jj * g.n_nt;
+    r.t1 = r.t0 + 1;
+    r.side = 0;
+    r.vs = 0;
+    r.row0 = g.blk[g.chunk_b0 + r.jj] * kBM;
+    r.a_row = r.jj * kBM;  // dZ rows are chunk-local
+  }
+  return r;
+}
+
+__device__ __forceinline__ void set_error(uint32_t* err, uint32_t bit) {
+  if (err) atomicOr(err, bit);
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(kThreads, 1)
+    k_gemm(const __grid_constant__ CUtensorMap mapA0, const __grid_constant__ CUtensorMap mapA1,
+           const __grid_constant__ CUtensorMap mapB, const GemmArgs g) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* smA = smem;
+  uint8_t* smB = smem + kStages * kAStageBytes;
+  Smem* sh = reinterpret_cast<Smem*>(smB + kStages * kBStageBytes);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&sh->full[s], 1);
+      mbar_init(&sh->empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&sh->acc_full[b], 1);
+      mbar_init(&sh->acc_empty[b], kEpiThreads);
+    }
+    mbar_init(&sh->mma_done, 1);
+    sh->abort = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&sh->tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+
+  const uint32_t tmem_base = sh->tmem_base;
+  volatile int* abort = &sh->abort;
+  const int nb = *g.nblk_dev;
+  const int n_units = unit_count<MODE>(g, nb);
+  const uint32_t b_bytes = static_cast<uint32_t>(g.bn) * kBK * 2;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&mapA0);
+      if (MODE == MODE_FWD) tma_prefetch_desc(&mapA1);
+      tma_prefetch_desc(&mapB);
+      int s = 0;
+      uint32_t ph = 0;
+      uint32_t issued = 0;           // stages that received at least one load
+      uint32_t last_par = 0;         // parity bit of the last load per stage
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < n_units; u += gridDim.x) {
+        const Unit un = unit_decode<MODE>(g, nb, u);
+        const CUtensorMap* mA = (MODE == MODE_FWD && un.side) ? &mapA1 : &mapA0;
+        for (int t = un.t0; ok && t < un.t1; ++t) {
+          const int b_row = t * g.bn;
+          for (int kb = 0; kb < g.nk; ++kb) {
+            if (!mbar_wait(&sh->empty[s], ph ^ 1u, abort)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(&sh->full[s], kAStageBytes + b_bytes);
+            tma_load_2d(smA + s * kAStageBytes, mA, &sh->full[s], kb * kBK, un.a_row);
+            tma_load_2d(smB + s * kBStageBytes, &mapB, &sh->full[s], kb * kBK, b_row);
+            issued |= 1u << s;
+            last_par = (last_par & ~(1u << s)) | (ph << s);
+            if (++s == kStages) {
+              s = 0;
+              ph ^= 1u;
+            }
+          }
+        }
+      }
+      if (!ok) {
+        set_error(g.err, ERRBIT_TIMEOUT);
+        *abort = 1;
+      }
+      // Drain: every load issued must have landed before the CTA exits.
+      volatile int no_abort = 0;
+      for (int st = 0; st < kStages; ++st)
+        if (issued & (1u << st)) mbar_wait(&sh->full[st], (last_par >> st) & 1u, &no_abort);
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16_f32(kBM, static_cast<uint32_t>(g.bn));
+      int s = 0;
+      uint32_t ph = 0;
+      int ab = 0;
+      uint32_t aph = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < n_units; u += gridDim.x) {
+        const Unit un = unit_decode<MODE>(g, nb, u);
+        for (int t = un.t0; ok && t < un.t1; ++t) {
+          if (!mbar_wait(&sh->acc_empty[ab], aph ^ 1u, abort)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(ab * kAccStride);
+          for (int kb = 0; kb < g.nk; ++kb) {
+            if (!mbar_wait(&sh->full[s], ph, abort)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t a_addr = smem_u32(smA + s * kAStageBytes);
+            const uint32_t b_addr = smem_u32(smB + s * kBStageBytes);
+#pragma unroll
+            for (int k = 0; k < kBK / 16; ++k) {
+              umma_bf16(d_tmem, sdesc_kmajor_sw128(a_addr + k * 32),
+                        sdesc_kmajor_sw128(b_addr + k * 32), idesc, (kb | k) != 0);
+            }
+            umma_commit(&sh->empty[s]);
+            if (++s == kStages) {
+              s = 0;
+              ph ^= 1u;
+            }
+          }
+          if (!ok) break;
+          umma_commit(&sh->acc_full[ab]);
+          if (++ab == 2) {
+            ab = 0;
+            aph ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        set_error(g.err, ERRBIT_TIMEOUT);
+        *abort = 1;
+      }
+      // Every MMA issued must complete before tensor memory is released.
+      umma_commit(&sh->mma_done);
+      volatile int no_abort = 0;
+      mbar_wait(&sh->mma_done, 0, &no_abort);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;  // TMEM lane quadrant this warp may access
+    const int r_in_tile = q * 32 + lane;
+    const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+    int ab = 0;
+    uint32_t aph = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; ok && u < n_units; u += gridDim.x) {
+      const Unit un = unit_decode<MODE>(g, nb, u);
+      const int64_t row = static_cast<int64_t>(un.row0) + r_in_tile;
+      const bool in_range = row < g.N;
+
+      // per-unit state
+      float m2 = -INFINITY, s_run = 0.f, s_comp = 0.f;  // FWD: running max / Kahan sum
+      int32_t y = -1;
+      float c_n = 0.f, lse2 = 0.f;
+      bool live = false;
+      if (MODE == MODE_FWD) {
+        y = in_range ? g.ids[row] : -1;
+      } else if (MODE == MODE_DZ) {
+        if (in_range) {
+          c_n = g.coef[row];
+          live = c_n != 0.f;
+          if (live) {
+            lse2 = g.lse[row] * kLog2e;
+            y = g.ids[row];
+          }
+        }
+      }
+
+      for (int t = un.t0; t < un.t1; ++t) {
+        // warp-uniform outcome: the tensor-memory loads below are .sync.aligned
+        if (!__all_sync(0xffffffffu, mbar_wait(&sh->acc_full[ab], aph, abort))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t tbase = lane_addr + static_cast<uint32_t>(ab * kAccStride);
+        const int64_t col_t = static_cast<int64_t>(t) * g.bn;
+
+        if (MODE == MODE_FWD) {
+          float ts = 0.f;  // this tile's sum, relative to m2
+#pragma unroll 1
+          for (int c = 0; c < kVocabTile / 32; ++c) {
+            uint32_t r[32];
+            tmem_ld32_wait(tbase + c * 32, r);
+            const int64_t col0 = col_t + c * 32;
+            float z[32];
+            float cm = -INFINITY;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              z[j] = (col0 + j < g.V) ? __uint_as_float(r[j]) * kLog2e : -INFINITY;
+              cm = fmaxf(cm, z[j]);
+            }
+            if (cm > m2) {
+              const float sc = ex2_approx(m2 - cm);
+              s_run *= sc;
+              s_comp *= sc;
+              ts *= sc;
+              m2 = cm;
+            }
+            float e[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) e[j] = ex2_approx(z[j] - m2);
+#pragma unroll
+            for (int w = 16; w >= 1; w >>= 1)
+#pragma unroll
+              for (int j = 0; j < w; ++j) e[j] += e[j + w];
+            ts += e[0];
+            const int64_t off = static_cast<int64_t>(y) - col0;
+            if (off >= 0 && off < 32) {
+              float zt = 0.f;
+#pragma unroll
+              for (int j = 0; j < 32; ++j)
+                if (j == off) zt = __uint_as_float(r[j]);
+              if (in_range) g.zy[static_cast<int64_t>(un.side) * g.N + row] = zt;
+            }
+          }
+          // Kahan-compensated accumulation of the tile sum
+          const float yk = ts - s_comp;
+          const float tk = s_run + yk;
+          s_comp = (tk - s_run) - yk;
+          s_run = tk;
+        } else if (MODE == MODE_DZ) {
+          __nv_bfloat16* dst =
+              g.dz + (static_cast<int64_t>(un.jj) * kBM + r_in_tile) * g.ldz;
+#pragma unroll 1
+          for (int c = 0; c < kVocabTile / 32; ++c) {
+            const int64_t col0 = col_t + c * 32;
+            if (col0 >= g.V) break;  // uniform across the warp
+            uint32_t r[32];
+            tmem_ld32_wait(tbase + c * 32, r);
+            float o[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              o[j] = live ? c_n * ex2_approx(fmaf(__uint_as_float(r[j]), kLog2e, -lse2)) : 0.f;
+            const int64_t off = static_cast<int64_t>(y) - col0;
+            if (off >= 0 && off < 32) {
+#pragma unroll
+              for (int j = 0; j < 32; ++j)
+                if (j == off) o[j] -= c_n;
+            }
+            uint32_t pk[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) pk[j] = pack_bf16x2(o[2 * j], o[2 * j + 1]);
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              if (col0 + 8 * v < g.V) {
+                *reinterpret_cast<uint4*>(dst + col0 + 8 * v) =
+                    make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+              }
+            }
+          }
+        } else {
+          const int ncc = g.bn / 32;
+#pragma unroll 1
+          for (int c = 0; c < ncc; ++c) {
+            const int64_t col0 = col_t + c * 32;
+            if (col0 >= g.d) break;  // uniform across the warp
+            uint32_t r[32];
+            tmem_ld32_wait(tbase + c * 32, r);
+            if (in_range) {
+              if (g.out_f32) {
+                float* dst = reinterpret_cast<float*>(g.out) + row * g.d + col0;
+#pragma unroll
+                for (int v = 0; v < 8; ++v)
+                  if (col0 + 4 * v < g.d)
+                    *reinterpret_cast<float4*>(dst + 4 * v) =
+                        make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
+                                    __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
+              } else {
+                __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(g.out) + row * g.d + col0;
+#pragma unroll
+                for (int v = 0; v < 4; ++v) {
+                  if (col0 + 8 * v < g.d) {
+                    uint4 pk;
+                    pk.x = pack_bf16x2(__uint_as_float(r[8 * v]), __uint_as_float(r[8 * v + 1]));
+                    pk.y = pack_bf16x2(__uint_as_float(r[8 * v + 2]), __uint_as_float(r[8 * v + 3]));
+                    pk.z = pack_bf16x2(__uint_as_float(r[8 * v + 4]), __uint_as_float(r[8 * v + 5]));
+                    pk.w = pack_bf16x2(__uint_as_float(r[8 * v + 6]), __uint_as_float(r[8 * v + 7]));
+                    *reinterpret_cast<uint4*>(dst + 8 * v) = pk;
+                  }
+                }
+              }
+            }
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(&sh->acc_empty[ab]);
+        if (++ab == 2) {
+          ab = 0;
+          aph ^= 1u;
+        }
+      }
+      if (!ok) break;
+      if (MODE == MODE_FWD) {
+        const int64_t pidx =
+            (static_cast<int64_t>(un.side) * g.nblk_max + un.jj) * g.n_vs + un.vs;
+        g.part[pidx * kBM + r_in_tile] = make_float2(m2, s_run);
+      }
+    }
+    if (!ok) {
+      set_error(g.err, ERRBIT_TIMEOUT);
+      *abort = 1;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) {
+    __syncwarp();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+}  // namespace
+
+size_t gemm_smem_bytes() { return kSmemBytes; }
+
+cudaError_t gemm_configure() {
+  cudaError_t e;
+  e = cudaFuncSetAttribute(k_gemm<MODE_FWD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kSmemBytes);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(k_gemm<MODE_DZ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kSmemBytes);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(k_gemm<MODE_DH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              kSmemBytes);
+}
+
+cudaError_t launch_gemm(int mode, const CUtensorMap& a0, const CUtensorMap& a1,
+                        const CUtensorMap& b, const GemmArgs& args, int grid,
+                        cudaStream_t stream) {
+  if (mode == MODE_FWD)
+    k_gemm<MODE_FWD><<<grid, kThreads, kSmemBytes, stream>>>(a0, a1, b, args);
+  else if (mode == MODE_DZ)
+    k_gemm<MODE_DZ><<<grid, kThreads, kSmemBytes, stream>>>(a0, a1, b, args);
+  else
+    k_gemm<MODE_DH><<<grid, kThreads, kSmemBytes, stream>>>(a0, a1, b, args);
+  return cudaGetLastError();
+}
+
+}  // namespace grpo

@@ -1,0 +1,555 @@
+// Host side of the C ABI: argument checks, the workspace plan, the chunk
+// scheduler over the flattened token axis, TMA descriptors and launches.
+#include <math.h>
+#include <string.h>
+
+#include <mutex>
+#include <vector>
+
+#include "../../include/grpo.h"
+#include "internal.h"
+
+using namespace grpo;
+
+namespace {
+
+constexpr size_t kAlign = 256;
+constexpr uint64_t kDefaultDzBudget = 4ull << 30;  // bytes of the bf16 dZ chunk
+constexpr int kFinishGrid = 608;                   // CTAs of the per-token finish kernel
+constexpr int kMaxSlices = 8;                      // vocab slices per block in the forward
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// ------------------------------------------------------------ profiling
+struct Profiler {
+  bool on = false;
+  std::vector<cudaEvent_t> ev;
+  std::vector<int> kind;
+  size_t used = 0;
+  int pending_kind = -1;
+};
+Profiler g_prof;
+constexpr size_t kMaxProfiled = 65536;
+
+const char* kKindNames[K_NUM_KINDS] = {
+    "advantages", "convert_bf16", "seq_count",  "block_plan",  "fwd_gemm_lse", "fwd_finish",
+    "fwd_reduce", "bwd_coef",     "transpose_w", "zero_rows",  "bwd_dz_gemm",  "bwd_dh_gemm"};
+
+void prof_begin(int k, cudaStream_t s) {
+  if (!g_prof.on || g_prof.used >= kMaxProfiled) return;
+  const size_t i = g_prof.used;
+  while (g_prof.ev.size() < 2 * (i + 1)) {
+    cudaEvent_t e;
+    if (cudaEventCreate(&e) != cudaSuccess) return;
+    g_prof.ev.push_back(e);
+  }
+  if (g_prof.kind.size() < i + 1) g_prof.kind.resize(i + 1);
+  cudaEventRecord(g_prof.ev[2 * i], s);
+  g_prof.pending_kind = k;
+}
+void prof_end(cudaStream_t s) {
+  if (!g_prof.on || g_prof.pending_kind < 0) return;
+  const size_t i = g_prof.used;
+  cudaEventRecord(g_prof.ev[2 * i + 1], s);
+  g_prof.kind[i] = g_prof.pending_kind;
+  g_prof.pending_kind = -1;
+  g_prof.used++;
+}
+
+#define LAUNCH(kind, stream, call)         \
+  do {                                     \
+    prof_begin(kind, stream);              \
+    cudaError_t e_ = (call);               \
+    prof_end(stream);                      \
+    if (e_ != cudaSuccess) return GRPO_ERR_CUDA; \
+  } while (0)
+
+// ------------------------------------------------------- device properties
+struct DeviceInfo {
+  int sms = 0;
+  bool configured = false;
+};
+std::mutex g_dev_mu;
+DeviceInfo g_dev[64];
+
+grpo_status device_info(int* sms) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return GRPO_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  DeviceInfo& di = g_dev[dev];
+  if (di.sms == 0) {
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0)
+      return GRPO_ERR_CUDA;
+    di.sms = v;
+  }
+  *sms = di.sms;
+  return GRPO_OK;
+}
+
+grpo_status configure_kernels() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return GRPO_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  if (!g_dev[dev].configured) {
+    if (gemm_configure() != cudaSuccess) return GRPO_ERR_CUDA;
+    g_dev[dev].configured = true;
+  }
+  return GRPO_OK;
+}
+
+// ------------------------------------------------------------- TMA maps
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// bf16 matrix [rows][inner] with row stride `ld` elements; box of
+// 64 x box_rows elements, 128-byte swizzle (the UMMA K-major layout).
+grpo_status make_map(CUtensorMap* m, const void* base, int64_t inner, int64_t rows, int64_t ld,
+                     int box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return GRPO_ERR_CUDA;
+  cuuint64_t gdim[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(rows)};
+  cuuint64_t gstride[1] = {static_cast<cuuint64_t>(ld) * 2};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), gdim, gstride,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? GRPO_OK : GRPO_ERR_UNSUPPORTED;
+}
+
+// ------------------------------------------------------------------ plan
+struct Plan {
+  int64_t N, d, V;
+  int B, T, G;
+  int sms;
+  int nblk_max;      // ceil(N / 128)
+  int n_vt;          // vocab tiles of 256
+  int n_vs;          // forward vocab slices
+  int nk_d;          // K blocks over d
+  int nk_v;          // K blocks over V
+  int bn_dh;         // dH tile width
+  int n_nt;          // dH column tiles
+  int chunk_nb;      // blocks per backward chunk
+  int n_chunks;
+  int64_t ldv;       // padded row length of dZ and W^T
+  bool f32;
+  // forward workspace offsets
+  size_t f_cnt, f_blk, f_inv, f_zy, f_part, f_partials, f_hp16, f_hr16, f_w16, f_total;
+  // backward workspace offsets
+  size_t b_cnt, b_blk, b_inv, b_coef, b_wt, b_dz, b_hp16, b_w16, b_total;
+};
+
+bool is_pow2ish_tile(int64_t d, int bn) { return d % bn == 0; }
+
+grpo_status validate_problem(const grpo_problem* p) {
+  if (!p) return GRPO_ERR_INVALID_ARG;
+  if (p->num_seqs < 1 || p->seq_len < 1 || p->group_size < 1) return GRPO_ERR_INVALID_ARG;
+  if (p->num_seqs % p->group_size != 0) return GRPO_ERR_INVALID_ARG;
+  if (p->N != static_cast<int64_t>(p->num_seqs) * p->seq_len) return GRPO_ERR_INVALID_ARG;
+  if (p->N > (static_cast<int64_t>(1) << 31) - 256) return GRPO_ERR_UNSUPPORTED;
+  if (p->d < 8 || p->V < 1 || p->V > (static_cast<int64_t>(1) << 31) - 256)
+    return GRPO_ERR_INVALID_ARG;
+  if (p->d % 8 != 0 || p->d > 65536) return GRPO_ERR_UNSUPPORTED;
+  if (!isfinite(p->beta) || !isfinite(p->eps)) return GRPO_ERR_INVALID_ARG;
+  if (p->dtype != GRPO_F32 && p->dtype != GRPO_BF16) return GRPO_ERR_INVALID_ARG;
+  if (p->chunk_rows < 0) return GRPO_ERR_INVALID_ARG;
+  if (p->compute_dW != 0) return GRPO_ERR_UNSUPPORTED;
+  return GRPO_OK;
+}
+
+int gcd_i(int a, int b) {
+  while (b) {
+    const int t = a % b;
+    a = b;
+    b = t;
+  }
+  return a;
+}
+
+grpo_status make_plan(const grpo_problem* p, Plan* pl) {
+  grpo_status st = validate_problem(p);
+  if (st != GRPO_OK) return st;
+  int sms = 0;
+  st = device_info(&sms);
+  if (st != GRPO_OK) return st;
+  Plan& P = *pl;
+  memset(&P, 0, sizeof(P));
+  P.N = p->N;
+  P.d = p->d;
+  P.V = p->V;
+  P.B = p->num_seqs;
+  P.T = p->seq_len;
+  P.G = p->group_size;
+  P.sms = sms;
+  P.f32 = p->dtype == GRPO_F32;
+  P.nblk_max = static_cast<int>(ceil_div(P.N, kBM));
+  P.n_vt = static_cast<int>(ceil_div(P.V, kVocabTile));
+  P.n_vs = P.n_vt < kMaxSlices ? P.n_vt : kMaxSlices;
+  P.nk_d = static_cast<int>(ceil_div(P.d, kBK));
+  P.nk_v = static_cast<int>(ceil_div(P.V, kBK));
+  P.ldv = (P.V + 7) / 8 * 8;
+  // widest dH tile (multiple of 32, <= 256) that divides d; else 256 with a clipped edge
+  P.bn_dh = 256;
+  for (int bn = 256; bn >= 32; bn -= 32)
+    if (is_pow2ish_tile(P.d, bn)) {
+      P.bn_dh = bn;
+      break;
+    }
+  P.n_nt = static_cast<int>(ceil_div(P.d, P.bn_dh));
+  // backward chunk: rows of the bf16 dZ buffer
+  if (p->chunk_rows > 0) {
+    P.chunk_nb = static_cast<int>(ceil_div(p->chunk_rows, kBM));
+  } else {
+    const uint64_t per_blk = static_cast<uint64_t>(kBM) * P.ldv * 2;
+    int64_t nbmax = static_cast<int64_t>(kDefaultDzBudget / per_blk);
+    if (nbmax < 1) nbmax = 1;
+    // prefer a multiple of the blocks that make the dH tile count a multiple of the SMs
+    const int m0 = sms / gcd_i(sms, P.n_nt);
+    if (nbmax >= m0) nbmax = nbmax / m0 * m0;
+    P.chunk_nb = static_cast<int>(nbmax);
+  }
+  if (P.chunk_nb > P.nblk_max) P.chunk_nb = P.nblk_max;
+  if (P.chunk_nb < 1) P.chunk_nb = 1;
+  P.n_chunks = static_cast<int>(ceil_div(P.nblk_max, P.chunk_nb));
+
+  size_t o = kAlign;  // control block first
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o = align_up(o + bytes, kAlign);
+    return at;
+  };
+  P.f_cnt = take(sizeof(int) * P.B);
+  P.f_blk = take(sizeof(int) * P.nblk_max);
+  P.f_inv = take(sizeof(int) * P.nblk_max);
+  P.f_zy = take(sizeof(float) * 2 * P.N);
+  P.f_part = take(sizeof(float2) * 2ull * P.nblk_max * P.n_vs * kBM);
+  P.f_partials = take(sizeof(double) * 3 * kFinishGrid);
+  if (P.f32) {
+    P.f_hp16 = take(2ull * P.N * P.d);
+    P.f_hr16 = take(2ull * P.N * P.d);
+    P.f_w16 = take(2ull * P.V * P.d);
+  }
+  P.f_total = o;
+
+  o = kAlign;
+  P.b_cnt = take(sizeof(int) * P.B);
+  P.b_blk = take(sizeof(int) * P.nblk_max);
+  P.b_inv = take(sizeof(int) * P.nblk_max);
+  P.b_coef = take(sizeof(float) * P.N);
+  P.b_wt = take(2ull * P.d * P.ldv);
+  P.b_dz = take(2ull * P.chunk_nb * kBM * P.ldv);
+  if (P.f32) {
+    P.b_hp16 = take(2ull * P.N * P.d);
+    P.b_w16 = take(2ull * P.V * P.d);
+  }
+  P.b_total = o;
+  return GRPO_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+// Control block at the start of every workspace.
+struct Ctrl {
+  uint32_t err;
+  int nblk;
+  float kl_scratch;
+};
+
+}  // namespace
+
+extern "C" {
+
+const char* grpo_status_string(grpo_status s) {
+  switch (s) {
+    case GRPO_OK: return "ok";
+    case GRPO_ERR_INVALID_ARG: return "invalid argument";
+    case GRPO_ERR_UNSUPPORTED: return "unsupported problem layout";
+    case GRPO_ERR_WORKSPACE: return "workspace null, misaligned or too small";
+    case GRPO_ERR_CUDA: return "CUDA runtime error";
+    case GRPO_ERR_TIMEOUT: return "device pipeline wait timed out";
+    case GRPO_ERR_BAD_TOKEN: return "valid token with id outside [0, V)";
+  }
+  return "unknown status";
+}
+
+grpo_status grpo_workspace_size(const grpo_problem* problem, size_t* fwd_bytes,
+                                size_t* bwd_bytes) {
+  Plan P;
+  const grpo_status st = make_plan(problem, &P);
+  if (st != GRPO_OK) return st;
+  if (fwd_bytes) *fwd_bytes = P.f_total;
+  if (bwd_bytes) *bwd_bytes = P.b_total;
+  return GRPO_OK;
+}
+
+grpo_status grpo_advantages(const float* rewards, int32_t num_seqs, int32_t group_size,
+                            float eps, int32_t std_unbiased, float* adv, cudaStream_t stream) {
+  if (!rewards || !adv || num_seqs < 1 || group_size < 1 || num_seqs % group_size != 0)
+    return GRPO_ERR_INVALID_ARG;
+  const int unb = std_unbiased ? 1 : 0;
+  if (group_size - unb < 1 || !isfinite(eps)) return GRPO_ERR_INVALID_ARG;
+  LAUNCH(K_ADVANTAGES, stream,
+         launch_advantages(rewards, num_seqs, group_size, eps, unb, adv, stream));
+  return GRPO_OK;
+}
+
+grpo_status grpo_loss_fwd(const grpo_problem* problem, const void* H_pol, const void* H_ref,
+                          const void* W, const int32_t* ids, const uint8_t* mask,
+                          const float* adv, float* logp_pol, float* logp_ref, float* lse_pol,
+                          float* loss, float* kl_mean, void* workspace, size_t workspace_bytes,
+                          cudaStream_t stream) {
+  grpo_status st = validate_problem(problem);
+  if (st != GRPO_OK) return st;
+  if (!H_pol || !H_ref || !W || !ids || !mask || !adv || !logp_pol || !logp_ref || !lse_pol ||
+      !loss)
+    return GRPO_ERR_INVALID_ARG;
+  Plan P;
+  if ((st = make_plan(problem, &P)) != GRPO_OK) return st;
+  if (!aligned16(H_pol) || !aligned16(H_ref) || !aligned16(W)) return GRPO_ERR_UNSUPPORTED;
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) % kAlign) != 0 ||
+      workspace_bytes < P.f_total)
+    return GRPO_ERR_WORKSPACE;
+  st = configure_kernels();
+  if (st != GRPO_OK) return st;
+
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  Ctrl* ctrl = reinterpret_cast<Ctrl*>(ws);
+  int* cnt = reinterpret_cast<int*>(ws + P.f_cnt);
+  int* blk = reinterpret_cast<int*>(ws + P.f_blk);
+  int* inv = reinterpret_cast<int*>(ws + P.f_inv);
+  float* zy = reinterpret_cast<float*>(ws + P.f_zy);
+  float2* part = reinterpret_cast<float2*>(ws + P.f_part);
+  double* partials = reinterpret_cast<double*>(ws + P.f_partials);
+
+  const void* hp = H_pol;
+  const void* hr = H_ref;
+  const void* w = W;
+  if (P.f32) {
+    __nv_bfloat16* hp16 = reinterpret_cast<__nv_bfloat16*>(ws + P.f_hp16);
+    __nv_bfloat16* hr16 = reinterpret_cast<__nv_bfloat16*>(ws + P.f_hr16);
+    __nv_bfloat16* w16 = reinterpret_cast<__nv_bfloat16*>(ws + P.f_w16);
+    LAUNCH(K_CONVERT, stream,
+           launch_convert_bf16(static_cast<const float*>(H_pol), hp16, P.N * P.d, stream));
+    LAUNCH(K_CONVERT, stream,
+           launch_convert_bf16(static_cast<const float*>(H_ref), hr16, P.N * P.d, stream));
+    LAUNCH(K_CONVERT, stream,
+           launch_convert_bf16(static_cast<const float*>(W), w16, P.V * P.d, stream));
+    hp = hp16;
+    hr = hr16;
+    w = w16;
+  }
+
+  CUtensorMap mHp, mHr, mW;
+  if ((st = make_map(&mHp, hp, P.d, P.N, P.d, kBM)) != GRPO_OK) return st;
+  if ((st = make_map(&mHr, hr, P.d, P.N, P.d, kBM)) != GRPO_OK) return st;
+  if ((st = make_map(&mW, w, P.d, P.V, P.d, kVocabTile)) != GRPO_OK) return st;
+
+  if (cudaMemsetAsync(ctrl, 0, sizeof(Ctrl), stream) != cudaSuccess) return GRPO_ERR_CUDA;
+  LAUNCH(K_SEQ_COUNT, stream,
+         launch_seq_count(mask, ids, P.B, P.T, P.V, cnt, &ctrl->err, stream));
+  LAUNCH(K_BLOCK_PLAN, stream,
+         launch_block_plan(mask, P.N, P.nblk_max, blk, inv, &ctrl->nblk, stream));
+
+  GemmArgs g;
+  memset(&g, 0, sizeof(g));
+  g.nblk_dev = &ctrl->nblk;
+  g.blk = blk;
+  g.n_vs = P.n_vs;
+  g.n_vt = P.n_vt;
+  g.bn = kVocabTile;
+  g.nk = P.nk_d;
+  g.nblk_max = P.nblk_max;
+  g.N = P.N;
+  g.d = P.d;
+  g.V = P.V;
+  g.ids = ids;
+  g.zy = zy;
+  g.part = part;
+  g.err = &ctrl->err;
+  const int64_t units = 2ll * P.nblk_max * P.n_vs;
+  const int grid = static_cast<int>(units < P.sms ? units : P.sms);
+  LAUNCH(K_FWD_GEMM, stream, launch_gemm(MODE_FWD, mHp, mHr, mW, g, grid, stream));
+
+  LAUNCH(K_FWD_FINISH, stream,
+         launch_fwd_finish(inv, mask, cnt, adv, zy, part, P.nblk_max, P.n_vs, P.N, P.B, P.T,
+                           logp_pol, logp_ref, lse_pol, partials, kFinishGrid, stream));
+  LAUNCH(K_FWD_REDUCE, stream,
+         launch_fwd_reduce(partials, kFinishGrid, cnt, P.B, problem->beta, loss,
+                           kl_mean ? kl_mean : &ctrl->kl_scratch, stream));
+  return GRPO_OK;
+}
+
+grpo_status grpo_loss_bwd(const grpo_problem* problem, const void* H_pol, const void* W,
+                          const int32_t* ids, const uint8_t* mask, const float* adv,
+                          const float* logp_pol, const float* logp_ref, const float* lse_pol,
+                          float grad_loss, void* dH, float* dW, void* workspace,
+                          size_t workspace_bytes, cudaStream_t stream) {
+  grpo_status st = validate_problem(problem);
+  if (st != GRPO_OK) return st;
+  if (!H_pol || !W || !ids || !mask || !adv || !logp_pol || !logp_ref || !lse_pol || !dH)
+    return GRPO_ERR_INVALID_ARG;
+  if (dW) return GRPO_ERR_UNSUPPORTED;
+  if (!isfinite(grad_loss)) return GRPO_ERR_INVALID_ARG;
+  Plan P;
+  if ((st = make_plan(problem, &P)) != GRPO_OK) return st;
+  if (!aligned16(H_pol) || !aligned16(W) || !aligned16(dH)) return GRPO_ERR_UNSUPPORTED;
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) % kAlign) != 0 ||
+      workspace_bytes < P.b_total)
+    return GRPO_ERR_WORKSPACE;
+  st = configure_kernels();
+  if (st != GRPO_OK) return st;
+
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  Ctrl* ctrl = reinterpret_cast<Ctrl*>(ws);
+  int* cnt = reinterpret_cast<int*>(ws + P.b_cnt);
+  int* blk = reinterpret_cast<int*>(ws + P.b_blk);
+  int* inv = reinterpret_cast<int*>(ws + P.b_inv);
+  float* coef = reinterpret_cast<float*>(ws + P.b_coef);
+  __nv_bfloat16* wt = reinterpret_cast<__nv_bfloat16*>(ws + P.b_wt);
+  __nv_bfloat16* dz = reinterpret_cast<__nv_bfloat16*>(ws + P.b_dz);
+
+  const void* hp = H_pol;
+  const void* w = W;
+  if (P.f32) {
+    __nv_bfloat16* hp16 = reinterpret_cast<__nv_bfloat16*>(ws + P.b_hp16);
+    __nv_bfloat16* w16 = reinterpret_cast<__nv_bfloat16*>(ws + P.b_w16);
+    LAUNCH(K_CONVERT, stream,
+           launch_convert_bf16(static_cast<const float*>(H_pol), hp16, P.N * P.d, stream));
+    LAUNCH(K_CONVERT, stream,
+           launch_convert_bf16(static_cast<const float*>(W), w16, P.V * P.d, stream));
+    hp = hp16;
+    w = w16;
+  }
+
+  CUtensorMap mHp, mW, mDz, mWt;
+  if ((st = make_map(&mHp, hp, P.d, P.N, P.d, kBM)) != GRPO_OK) return st;
+  if ((st = make_map(&mW, w, P.d, P.V, P.d, kVocabTile)) != GRPO_OK) return st;
+  if ((st = make_map(&mDz, dz, P.V, static_cast<int64_t>(P.chunk_nb) * kBM, P.ldv, kBM)) !=
+      GRPO_OK)
+    return st;
+  if ((st = make_map(&mWt, wt, P.V, P.d, P.ldv, P.bn_dh)) != GRPO_OK) return st;
+
+  if (cudaMemsetAsync(ctrl, 0, sizeof(Ctrl), stream) != cudaSuccess) return GRPO_ERR_CUDA;
+  LAUNCH(K_SEQ_COUNT, stream,
+         launch_seq_count(mask, ids, P.B, P.T, P.V, cnt, &ctrl->err, stream));
+  LAUNCH(K_BLOCK_PLAN, stream,
+         launch_block_plan(mask, P.N, P.nblk_max, blk, inv, &ctrl->nblk, stream));
+  LAUNCH(K_BWD_COEF, stream,
+         launch_bwd_coef(mask, cnt, adv, logp_pol, logp_ref, P.N, P.B, P.T, problem->beta,
+                         grad_loss, coef, stream));
+  LAUNCH(K_TRANSPOSE_W, stream, launch_transpose_w(W, P.f32, P.V, P.d, wt, P.ldv, stream));
+  LAUNCH(K_ZERO_ROWS, stream, launch_zero_invalid_rows(inv, P.N, P.d, dH, P.f32, stream));
+
+  GemmArgs g;
+  memset(&g, 0, sizeof(g));
+  g.nblk_dev = &ctrl->nblk;
+  g.blk = blk;
+  g.n_vt = P.n_vt;
+  g.n_vs = 1;
+  g.n_nt = P.n_nt;
+  g.chunk_nb = P.chunk_nb;
+  g.nblk_max = P.nblk_max;
+  g.N = P.N;
+  g.d = P.d;
+  g.V = P.V;
+  g.ids = ids;
+  g.lse = lse_pol;
+  g.coef = coef;
+  g.dz = dz;
+  g.ldz = P.ldv;
+  g.out = dH;
+  g.out_f32 = P.f32 ? 1 : 0;
+  g.err = &ctrl->err;
+  const int64_t dz_units = static_cast<int64_t>(P.chunk_nb) * P.n_vt;
+  const int64_t dh_units = static_cast<int64_t>(P.chunk_nb) * P.n_nt;
+  const int grid_dz = static_cast<int>(dz_units < P.sms ? dz_units : P.sms);
+  const int grid_dh = static_cast<int>(dh_units < P.sms ? dh_units : P.sms);
+  for (int c = 0; c < P.n_chunks; ++c) {
+    g.chunk_b0 = c * P.chunk_nb;
+    GemmArgs gz = g;
+    gz.bn = kVocabTile;
+    gz.nk = P.nk_d;
+    LAUNCH(K_BWD_DZ_GEMM, stream, launch_gemm(MODE_DZ, mHp, mHp, mW, gz, grid_dz, stream));
+    GemmArgs gh = g;
+    gh.bn = P.bn_dh;
+    gh.nk = P.nk_v;
+    LAUNCH(K_BWD_DH_GEMM, stream, launch_gemm(MODE_DH, mDz, mDz, mWt, gh, grid_dh, stream));
+  }
+  return GRPO_OK;
+}
+
+grpo_status grpo_get_device_status(void* workspace, cudaStream_t stream) {
+  if (!workspace) return GRPO_ERR_INVALID_ARG;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return GRPO_ERR_CUDA;
+  uint32_t err = 0;
+  Ctrl* ctrl = static_cast<Ctrl*>(workspace);
+  if (cudaMemcpy(&err, &ctrl->err, sizeof(err), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return GRPO_ERR_CUDA;
+  if (err) {
+    const uint32_t zero = 0;
+    if (cudaMemcpy(&ctrl->err, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
+      return GRPO_ERR_CUDA;
+  }
+  if (err & ERRBIT_TIMEOUT) return GRPO_ERR_TIMEOUT;
+  if (err & ERRBIT_BAD_TOKEN) return GRPO_ERR_BAD_TOKEN;
+  return GRPO_OK;
+}
+
+grpo_status grpo_profile_enable(int32_t on) {
+  g_prof.on = on != 0;
+  return GRPO_OK;
+}
+
+grpo_status grpo_profile_collect(double* ms, int64_t* launches, int32_t n_kinds) {
+  if (n_kinds < 0 || (n_kinds > 0 && (!ms || !launches))) return GRPO_ERR_INVALID_ARG;
+  for (int k = 0; k < n_kinds; ++k) {
+    ms[k] = 0.0;
+    launches[k] = 0;
+  }
+  grpo_status st = GRPO_OK;
+  for (size_t i = 0; i < g_prof.used; ++i) {
+    if (cudaEventSynchronize(g_prof.ev[2 * i + 1]) != cudaSuccess) {
+      st = GRPO_ERR_CUDA;
+      continue;
+    }
+    float t = 0.f;
+    if (cudaEventElapsedTime(&t, g_prof.ev[2 * i], g_prof.ev[2 * i + 1]) != cudaSuccess) {
+      st = GRPO_ERR_CUDA;
+      continue;
+    }
+    const int k = g_prof.kind[i];
+    if (k < n_kinds) {
+      ms[k] += t;
+      launches[k] += 1;
+    }
+  }
+  g_prof.used = 0;
+  return st;
+}
+
+int32_t grpo_profile_kind_count(void) { return K_NUM_KINDS; }
+
+const char* grpo_profile_kind_name(int32_t kind) {
+  if (kind < 0 || kind >= K_NUM_KINDS) return "unknown";
+  return kKindNames[kind];
+}
+
+}  // extern "C"

@@ -1,0 +1,94 @@
+// Internal interfaces between the host planner (grpo_api.cu) and the kernel
+// translation units. Not part of the public C ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace grpo {
+
+// Device error word bits (kept in the first bytes of every workspace).
+enum : uint32_t { ERRBIT_TIMEOUT = 1u, ERRBIT_BAD_TOKEN = 2u };
+
+constexpr int kBM = 128;         // rows per output tile (one TMEM lane per row)
+constexpr int kBK = 64;          // bf16 K elements per 128-byte swizzled row
+constexpr int kVocabTile = 256;  // vocab columns per tile in the logit GEMMs
+
+enum GemmMode : int { MODE_FWD = 0, MODE_DZ = 1, MODE_DH = 2 };
+
+// Everything a GEMM launch needs besides its tensor maps.
+struct GemmArgs {
+  const int* nblk_dev;    // number of 128-row blocks holding a valid token (device)
+  const int* blk;         // compacted list of those blocks (original block index)
+  int n_vs;               // MODE_FWD: vocab slices per block
+  int n_vt;               // vocab tiles of kVocabTile columns
+  int n_nt;               // MODE_DH: output column tiles
+  int bn;                 // output tile width (MODE_FWD/DZ: 256)
+  int nk;                 // 64-wide K blocks
+  int chunk_b0;           // MODE_DZ/DH: first compacted block of the chunk
+  int chunk_nb;           // MODE_DZ/DH: blocks per chunk
+  int nblk_max;           // ceil(N / 128)
+  int64_t N, d, V;
+  const int32_t* ids;
+  float* zy;              // MODE_FWD: target logits [2][N]
+  float2* part;           // MODE_FWD: (max2, sumexp2) [2 * nblk_max][n_vs][128]
+  const float* lse;       // MODE_DZ: policy logsumexp [N]
+  const float* coef;      // MODE_DZ: c_n [N]
+  __nv_bfloat16* dz;      // MODE_DZ: chunk of dZ, [chunk_nb * 128][ldz]
+  int64_t ldz;
+  void* out;              // MODE_DH: dH [N][d]
+  int out_f32;
+  uint32_t* err;          // device error word
+};
+
+// Profiling kinds (one per kernel the library launches).
+enum KernelKind : int {
+  K_ADVANTAGES = 0,
+  K_CONVERT,
+  K_SEQ_COUNT,
+  K_BLOCK_PLAN,
+  K_FWD_GEMM,
+  K_FWD_FINISH,
+  K_FWD_REDUCE,
+  K_BWD_COEF,
+  K_TRANSPOSE_W,
+  K_ZERO_ROWS,
+  K_BWD_DZ_GEMM,
+  K_BWD_DH_GEMM,
+  K_NUM_KINDS
+};
+
+// ------------------------------------------------------------- gemm_tc.cu
+size_t gemm_smem_bytes();
+cudaError_t gemm_configure();  // sets the dynamic shared memory limit once
+cudaError_t launch_gemm(int mode, const CUtensorMap& a0, const CUtensorMap& a1,
+                        const CUtensorMap& b, const GemmArgs& args, int grid,
+                        cudaStream_t stream);
+
+// ---------------------------------------------------------------- rows.cu
+cudaError_t launch_advantages(const float* rewards, int B, int G, float eps, int unbiased,
+                              float* adv, cudaStream_t s);
+cudaError_t launch_convert_bf16(const float* src, __nv_bfloat16* dst, int64_t n,
+                                cudaStream_t s);
+cudaError_t launch_seq_count(const uint8_t* mask, const int32_t* ids, int B, int T, int64_t V,
+                             int* cnt, uint32_t* err, cudaStream_t s);
+cudaError_t launch_block_plan(const uint8_t* mask, int64_t N, int nblk, int* blk, int* inv,
+                              int* nblk_dev, cudaStream_t s);
+cudaError_t launch_fwd_finish(const int* inv, const uint8_t* mask, const int* cnt,
+                              const float* adv, const float* zy, const float2* part,
+                              int nblk_max, int n_vs, int64_t N, int B, int T, float* logp_pol,
+                              float* logp_ref, float* lse_pol, double* partials, int grid,
+                              cudaStream_t s);
+cudaError_t launch_fwd_reduce(const double* partials, int nparts, const int* cnt, int B,
+                              float beta, float* loss, float* kl_mean, cudaStream_t s);
+cudaError_t launch_bwd_coef(const uint8_t* mask, const int* cnt, const float* adv,
+                            const float* logp_pol, const float* logp_ref, int64_t N, int B,
+                            int T, float beta, float grad, float* coef, cudaStream_t s);
+cudaError_t launch_transpose_w(const void* W, int w_f32, int64_t V, int64_t d,
+                               __nv_bfloat16* Wt, int64_t ldwt, cudaStream_t s);
+cudaError_t launch_zero_invalid_rows(const int* inv, int64_t N, int64_t d, void* out,
+                                     int out_f32, cudaStream_t s);
+
+}  // namespace grpo

@@ -1,0 +1,395 @@
+// Row-wise and small kernels of the GRPO loss path: group advantages, the
+// row plan (per-sequence counts and the list of 128-row blocks holding a
+// valid token), the per-token loss terms with deterministic float64
+// reductions, the backward coefficients, the W transpose and fills.
+#include <algorithm>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace grpo {
+
+namespace {
+
+__device__ __forceinline__ double warp_sum_d(double v) {
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+__device__ __forceinline__ int warp_sum_i(int v) {
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// ------------------------------------------------------------- advantages
+// One warp per group of G contiguous rewards; mean and std in float64.
+__global__ void k_advantages(const float* __restrict__ r, int B, int G, float eps, int unbiased,
+                             float* __restrict__ adv) {
+  const int grp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (grp >= B / G) return;
+  const float* rg = r + static_cast<int64_t>(grp) * G;
+  double s = 0.0;
+  for (int i = lane; i < G; i += 32) s += static_cast<double>(rg[i]);
+  const double mean = warp_sum_d(s) / G;
+  double v = 0.0;
+  for (int i = lane; i < G; i += 32) {
+    const double dd = static_cast<double>(rg[i]) - mean;
+    v += dd * dd;
+  }
+  const double sd = sqrt(warp_sum_d(v) / (G - unbiased));
+  const double den = sd + static_cast<double>(eps);
+  for (int i = lane; i < G; i += 32)
+    adv[static_cast<int64_t>(grp) * G + i] =
+        static_cast<float>((static_cast<double>(rg[i]) - mean) / den);
+}
+
+// --------------------------------------------------------------- convert
+__global__ void k_convert_bf16(const float* __restrict__ src, __nv_bfloat16* __restrict__ dst,
+                               int64_t n) {
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i * 4 < n;
+       i += stride) {
+    const int64_t e = i * 4;
+    if (e + 4 <= n) {
+      const float4 v = *reinterpret_cast<const float4*>(src + e);
+      uint2 o;
+      o.x = pack_bf16x2(v.x, v.y);
+      o.y = pack_bf16x2(v.z, v.w);
+      *reinterpret_cast<uint2*>(dst + e) = o;
+    } else {
+      for (int64_t k = e; k < n; ++k) dst[k] = __float2bfloat16_rn(src[k]);
+    }
+  }
+}
+
+// ------------------------------------------------------------- seq count
+// One CTA per sequence: cnt_b = number of valid tokens; valid tokens whose id
+// is outside [0, V) raise the bad-token bit.
+__global__ void k_seq_count(const uint8_t* __restrict__ mask, const int32_t* __restrict__ ids,
+                            int T, int64_t V, int* __restrict__ cnt, uint32_t* err) {
+  __shared__ int wsum[32];
+  const int b = blockIdx.x;
+  const int64_t r0 = static_cast<int64_t>(b) * T;
+  int c = 0;
+  bool bad = false;
+  for (int t = threadIdx.x; t < T; t += blockDim.x) {
+    if (mask[r0 + t]) {
+      ++c;
+      const int32_t y = ids[r0 + t];
+      bad |= (y < 0) || (static_cast<int64_t>(y) >= V);
+    }
+  }
+  if (bad) atomicOr(err, ERRBIT_BAD_TOKEN);
+  c = warp_sum_i(c);
+  if ((threadIdx.x & 31) == 0) wsum[threadIdx.x >> 5] = c;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    int v = threadIdx.x < (blockDim.x >> 5) ? wsum[threadIdx.x] : 0;
+    v = warp_sum_i(v);
+    if (threadIdx.x == 0) cnt[b] = v;
+  }
+}
+
+// ------------------------------------------------------------ block plan
+// Single CTA of 1024 threads: flag each 128-row block that holds a valid
+// token, then compact the flagged blocks in order (block-wide scan).
+__global__ void __launch_bounds__(1024) k_block_plan(const uint8_t* __restrict__ mask, int64_t N,
+                                                     int nblk, int* __restrict__ blk,
+                                                     int* __restrict__ inv, int* nblk_dev) {
+  __shared__ int wtot[32];
+  __shared__ int base;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (threadIdx.x == 0) base = 0;
+  __syncthreads();
+  const bool aligned = (reinterpret_cast<uintptr_t>(mask) & 15) == 0;
+  for (int k0 = 0; k0 < nblk; k0 += 1024) {
+    const int k = k0 + threadIdx.x;
+    int flag = 0;
+    if (k < nblk) {
+      const int64_t r0 = static_cast<int64_t>(k) * kBM;
+      const int64_t r1 = min(N, r0 + kBM);
+      if (aligned && r1 - r0 == kBM) {
+        const uint4* p = reinterpret_cast<const uint4*>(mask + r0);
+        uint32_t acc = 0;
+#pragma unroll
+        for (int i = 0; i < kBM / 16; ++i) {
+          const uint4 v = p[i];
+          acc |= v.x | v.y | v.z | v.w;
+        }
+        flag = acc != 0;
+      } else {
+        for (int64_t r = r0; r < r1; ++r) flag |= mask[r] != 0;
+      }
+    }
+    // inclusive scan of flag across the CTA
+    int x = flag;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    if (lane == 31) wtot[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+      int w = wtot[lane];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, w, o);
+        if (lane >= o) w += y;
+      }
+      wtot[lane] = w;  // inclusive warp totals
+    }
+    __syncthreads();
+    const int excl = x - flag + (warp > 0 ? wtot[warp - 1] : 0);
+    if (k < nblk) {
+      inv[k] = flag ? base + excl : -1;
+      if (flag) blk[base + excl] = k;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) base += wtot[31];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) *nblk_dev = base;
+}
+
+// ------------------------------------------------------------ fwd finish
+// Merge the vocab-slice partials into each row's logsumexp, form q, p, the
+// KL estimator and the weighted loss terms. Per-CTA float64 partial sums
+// (sum w*A, sum w*KL, sum m*KL) go to `partials` for a fixed-order final sum.
+__device__ __forceinline__ float merge_lse(const float2* p, int n_vs) {
+  float M = -INFINITY;
+  for (int v = 0; v < n_vs; ++v) M = fmaxf(M, p[static_cast<int64_t>(v) * kBM].x);
+  float S = 0.f;
+  for (int v = 0; v < n_vs; ++v) {
+    const float2 e = p[static_cast<int64_t>(v) * kBM];
+    S += e.y * exp2f(e.x - M);
+  }
+  return (M + log2f(S)) * 0.69314718055994531f;
+}
+
+__global__ void k_fwd_finish(const int* __restrict__ inv, const uint8_t* __restrict__ mask,
+                             const int* __restrict__ cnt, const float* __restrict__ adv,
+                             const float* __restrict__ zy, const float2* __restrict__ part,
+                             int nblk_max, int n_vs, int64_t N, int B, int T,
+                             float* __restrict__ logp_pol, float* __restrict__ logp_ref,
+                             float* __restrict__ lse_pol, double* __restrict__ partials) {
+  __shared__ double red[3][32];
+  double sa = 0.0, sk = 0.0, sm = 0.0;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t n = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; n < N;
+       n += stride) {
+    const int k = static_cast<int>(n / kBM);
+    const int j = inv[k];
+    float lp = 0.f, lr = 0.f, ls = 0.f;
+    if (j >= 0) {
+      const int r = static_cast<int>(n - static_cast<int64_t>(k) * kBM);
+      const float2* pp = part + (static_cast<int64_t>(j) * n_vs) * kBM + r;
+      const float2* pr = part + ((static_cast<int64_t>(nblk_max) + j) * n_vs) * kBM + r;
+      ls = merge_lse(pp, n_vs);
+      if (mask[n]) {
+        const float lse_r = merge_lse(pr, n_vs);
+        const float q = zy[n] - ls;
+        const float p = zy[N + n] - lse_r;
+        lp = q;
+        lr = p;
+        const float x = p - q;
+        const float kl = expm1f(x) - x;
+        const int b = static_cast<int>(n / T);
+        const double w = 1.0 / (static_cast<double>(B) * max(cnt[b], 1));
+        sa += w * static_cast<double>(adv[b]);
+        sk += w * static_cast<double>(kl);
+        sm += static_cast<double>(kl);
+      }
+    }
+    logp_pol[n] = lp;
+    logp_ref[n] = lr;
+    lse_pol[n] = ls;
+  }
+  sa = warp_sum_d(sa);
+  sk = warp_sum_d(sk);
+  sm = warp_sum_d(sm);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (lane == 0) {
+    red[0][warp] = sa;
+    red[1][warp] = sk;
+    red[2][warp] = sm;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    const int nw = blockDim.x >> 5;
+    double a = lane < nw ? red[0][lane] : 0.0;
+    double b = lane < nw ? red[1][lane] : 0.0;
+    double c = lane < nw ? red[2][lane] : 0.0;
+    a = warp_sum_d(a);
+    b = warp_sum_d(b);
+    c = warp_sum_d(c);
+    if (lane == 0) {
+      partials[3 * blockIdx.x + 0] = a;
+      partials[3 * blockIdx.x + 1] = b;
+      partials[3 * blockIdx.x + 2] = c;
+    }
+  }
+}
+
+// Single warp: fixed-order sum of the per-CTA partials.
+__global__ void k_fwd_reduce(const double* __restrict__ partials, int nparts,
+                             const int* __restrict__ cnt, int B, float beta, float* loss,
+                             float* kl_mean) {
+  const int lane = threadIdx.x;
+  double a = 0.0, k = 0.0, m = 0.0, c = 0.0;
+  for (int i = lane; i < nparts; i += 32) {
+    a += partials[3 * i + 0];
+    k += partials[3 * i + 1];
+    m += partials[3 * i + 2];
+  }
+  for (int i = lane; i < B; i += 32) c += static_cast<double>(cnt[i]);
+  a = warp_sum_d(a);
+  k = warp_sum_d(k);
+  m = warp_sum_d(m);
+  c = warp_sum_d(c);
+  if (lane == 0) {
+    *loss = static_cast<float>(-a + static_cast<double>(beta) * k);
+    if (kl_mean) *kl_mean = c > 0.0 ? static_cast<float>(m / c) : 0.f;
+  }
+}
+
+// -------------------------------------------------------- bwd coefficient
+// c_n = g * w_n * (A_b + beta * (exp(p - q) - 1)) at valid rows, 0 elsewhere.
+__global__ void k_bwd_coef(const uint8_t* __restrict__ mask, const int* __restrict__ cnt,
+                           const float* __restrict__ adv, const float* __restrict__ logp_pol,
+                           const float* __restrict__ logp_ref, int64_t N, int B, int T,
+                           float beta, float grad, float* __restrict__ coef) {
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t n = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; n < N;
+       n += stride) {
+    float c = 0.f;
+    if (mask[n]) {
+      const int b = static_cast<int>(n / T);
+      const double w = 1.0 / (static_cast<double>(B) * max(cnt[b], 1));
+      const float x = logp_ref[n] - logp_pol[n];
+      c = static_cast<float>(static_cast<double>(grad) * w *
+                             (static_cast<double>(adv[b]) +
+                              static_cast<double>(beta) * static_cast<double>(expm1f(x))));
+    }
+    coef[n] = c;
+  }
+}
+
+// ------------------------------------------------------------- transpose
+// Wt[c][r] = bf16(W[r][c]) for W [V, d] (bf16 or f32), 32x32 tiles.
+template <typename Tin>
+__global__ void k_transpose_w(const Tin* __restrict__ W, int64_t V, int64_t d,
+                              __nv_bfloat16* __restrict__ Wt, int64_t ldwt) {
+  __shared__ float tile[32][33];
+  const int64_t r0 = static_cast<int64_t>(blockIdx.x) * 32;
+  const int64_t c0 = static_cast<int64_t>(blockIdx.y) * 32;
+  for (int i = threadIdx.y; i < 32; i += blockDim.y) {
+    const int64_t r = r0 + i, c = c0 + threadIdx.x;
+    float v = 0.f;
+    if (r < V && c < d) {
+      if constexpr (sizeof(Tin) == 4)
+        v = W[r * d + c];
+      else
+        v = __bfloat162float(W[r * d + c]);
+    }
+    tile[i][threadIdx.x] = v;
+  }
+  __syncthreads();
+  for (int i = threadIdx.y; i < 32; i += blockDim.y) {
+    const int64_t c = c0 + i, r = r0 + threadIdx.x;
+    if (c < d && r < V) Wt[c * ldwt + r] = __float2bfloat16_rn(tile[threadIdx.x][i]);
+  }
+}
+
+// ------------------------------------------------------------ zero rows
+// Zero the output rows of every 128-row block that holds no valid token.
+__global__ void k_zero_invalid_rows(const int* __restrict__ inv, int64_t N, int64_t row_bytes,
+                                    uint8_t* __restrict__ out) {
+  const int k = blockIdx.x;
+  if (inv[k] >= 0) return;
+  const int64_t r0 = static_cast<int64_t>(k) * kBM;
+  const int64_t r1 = min(N, r0 + kBM);
+  const int64_t n16 = (r1 - r0) * row_bytes / 16;
+  uint4* p = reinterpret_cast<uint4*>(out + r0 * row_bytes);
+  for (int64_t i = threadIdx.x; i < n16; i += blockDim.x) p[i] = make_uint4(0, 0, 0, 0);
+}
+
+}  // namespace
+
+cudaError_t launch_advantages(const float* rewards, int B, int G, float eps, int unbiased,
+                              float* adv, cudaStream_t s) {
+  const int groups = B / G;
+  const int threads = 128;
+  const int blocks = (groups * 32 + threads - 1) / threads;
+  k_advantages<<<blocks, threads, 0, s>>>(rewards, B, G, eps, unbiased, adv);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_convert_bf16(const float* src, __nv_bfloat16* dst, int64_t n,
+                                cudaStream_t s) {
+  const int64_t vec = (n + 3) / 4;
+  const int blocks = static_cast<int>(std::min<int64_t>((vec + 255) / 256, 8192));
+  k_convert_bf16<<<blocks, 256, 0, s>>>(src, dst, n);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_seq_count(const uint8_t* mask, const int32_t* ids, int B, int T, int64_t V,
+                             int* cnt, uint32_t* err, cudaStream_t s) {
+  k_seq_count<<<B, 256, 0, s>>>(mask, ids, T, V, cnt, err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_block_plan(const uint8_t* mask, int64_t N, int nblk, int* blk, int* inv,
+                              int* nblk_dev, cudaStream_t s) {
+  k_block_plan<<<1, 1024, 0, s>>>(mask, N, nblk, blk, inv, nblk_dev);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fwd_finish(const int* inv, const uint8_t* mask, const int* cnt,
+                              const float* adv, const float* zy, const float2* part,
+                              int nblk_max, int n_vs, int64_t N, int B, int T, float* logp_pol,
+                              float* logp_ref, float* lse_pol, double* partials, int grid,
+                              cudaStream_t s) {
+  k_fwd_finish<<<grid, 256, 0, s>>>(inv, mask, cnt, adv, zy, part, nblk_max, n_vs, N, B, T,
+                                    logp_pol, logp_ref, lse_pol, partials);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fwd_reduce(const double* partials, int nparts, const int* cnt, int B,
+                              float beta, float* loss, float* kl_mean, cudaStream_t s) {
+  k_fwd_reduce<<<1, 32, 0, s>>>(partials, nparts, cnt, B, beta, loss, kl_mean);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_coef(const uint8_t* mask, const int* cnt, const float* adv,
+                            const float* logp_pol, const float* logp_ref, int64_t N, int B,
+                            int T, float beta, float grad, float* coef, cudaStream_t s) {
+  const int blocks = static_cast<int>(std::min<int64_t>((N + 255) / 256, 4096));
+  k_bwd_coef<<<blocks, 256, 0, s>>>(mask, cnt, adv, logp_pol, logp_ref, N, B, T, beta, grad,
+                                    coef);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_transpose_w(const void* W, int w_f32, int64_t V, int64_t d,
+                               __nv_bfloat16* Wt, int64_t ldwt, cudaStream_t s) {
+  dim3 grid(static_cast<unsigned>((V + 31) / 32), static_cast<unsigned>((d + 31) / 32));
+  dim3 block(32, 8);
+  if (w_f32)
+    k_transpose_w<float><<<grid, block, 0, s>>>(static_cast<const float*>(W), V, d, Wt, ldwt);
+  else
+    k_transpose_w<__nv_bfloat16>
+        <<<grid, block, 0, s>>>(static_cast<const __nv_bfloat16*>(W), V, d, Wt, ldwt);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_zero_invalid_rows(const int* inv, int64_t N, int64_t d, void* out,
+                                     int out_f32, cudaStream_t s) {
+  const int nblk = static_cast<int>((N + kBM - 1) / kBM);
+  k_zero_invalid_rows<<<nblk, 256, 0, s>>>(inv, N, d * (out_f32 ? 4 : 2),
+                                           static_cast<uint8_t*>(out));
+  return cudaGetLastError();
+}
+
+}  // namespace grpo

@@ -1,0 +1,177 @@
+/*
+ * grpo.h - C ABI of the GB300 (sm_103a) memory-efficient GRPO loss library.
+ *
+ * The library computes the "linear" GRPO loss of the Unsloth GRPO blog
+ * (zjt100.com translation, "Unsloth 高效 GRPO 算法" and "GRPO 的数学和发现的问题"):
+ * the lm_head projection, the log-softmax and the GRPO objective fused over
+ * the flattened (generations x completion length) token axis, without ever
+ * forming the [N, V] logits. The backward pass recomputes the logit tiles
+ * (Unsloth "grpo-long-context" page, offloaded log-softmax section) and
+ * walks the token axis in chunks (same page, flattened sequence chunking,
+ * Equation 3).
+ *
+ * Notation. B = num_seqs sequences of seq_len = T tokens; row n = b*T + t
+ * (the G generations of a prompt are contiguous sequences). N = B*T rows, d
+ * = hidden size, V = vocab. H_pol / H_ref are the policy / frozen reference
+ * hidden states [N, d]; W is the lm_head weight [V, d] (logits = H W^T);
+ * ids[n] is the token scored at row n (the caller has already shifted);
+ * mask[n] in {0,1}; cnt_b = sum_t mask[b*T+t];
+ * w_n = mask[n] / (B * max(cnt_b, 1)).
+ * q_n = log softmax(H_pol[n] W^T)[ids[n]], p_n likewise from H_ref,
+ * x_n = p_n - q_n, KL_n = exp(x_n) - x_n - 1 (reverse-KL estimator).
+ * loss = sum_n w_n * (-(A_b - beta * KL_n)), the value of
+ * exp(q - q.detach()) * A being 1.
+ *
+ * Conventions shared by every call:
+ *  - Every tensor argument is a DEVICE pointer owned by the caller,
+ *    row-major and contiguous, 16-byte aligned. The library never
+ *    allocates device memory; scratch space is the caller's workspace.
+ *  - Calls are asynchronous on `stream`; nothing synchronises except
+ *    grpo_get_device_status and grpo_profile_collect. A workspace must not
+ *    be shared by calls that may run concurrently.
+ *  - The return value reports host-detectable errors, found before any
+ *    launch (bad sizes, null pointers, short workspace). Errors found on the
+ *    device (a valid token with an id outside [0, V), a pipeline wait that
+ *    timed out) are recorded in the workspace's error word and read by
+ *    grpo_get_device_status; the outputs of that call are then unspecified.
+ *  - Outputs are overwritten, never accumulated.
+ */
+#ifndef GRPO_H
+#define GRPO_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same definition as the CUDA runtime's stream handle. */
+typedef struct CUstream_st *cudaStream_t;
+
+typedef enum grpo_status {
+  GRPO_OK = 0,
+  GRPO_ERR_INVALID_ARG = 1,  /* null pointer, inconsistent sizes, bad group */
+  GRPO_ERR_UNSUPPORTED = 2,  /* a layout the kernels do not handle (d % 8 != 0) */
+  GRPO_ERR_WORKSPACE = 3,    /* workspace null, misaligned or too small */
+  GRPO_ERR_CUDA = 4,         /* a CUDA runtime call failed */
+  GRPO_ERR_TIMEOUT = 5,      /* device: a bounded pipeline wait expired */
+  GRPO_ERR_BAD_TOKEN = 6     /* device: a valid token id outside [0, V) */
+} grpo_status;
+
+/* Element type of H_pol, H_ref, W and dH. GRPO_F32 inputs are rounded to
+ * bf16 for the tensor-core products; accumulation is float32 either way. */
+typedef enum grpo_dtype { GRPO_F32 = 0, GRPO_BF16 = 1 } grpo_dtype;
+
+typedef struct grpo_problem {
+  int64_t N;            /* rows = num_seqs * seq_len */
+  int64_t d;            /* hidden size, multiple of 8 */
+  int64_t V;            /* vocab size */
+  int32_t num_seqs;     /* B */
+  int32_t seq_len;      /* T */
+  int32_t group_size;   /* G generations per prompt (divides B) */
+  float beta;           /* KL weight, the pages use 0.04 */
+  float eps;            /* advantage denominator guard, e.g. 1e-4 */
+  int32_t std_unbiased; /* 1: group std with Bessel's correction, 0: without */
+  int64_t chunk_rows;   /* backward token chunk; 0 = chosen from a 4 GiB dZ budget */
+  int32_t compute_dW;   /* must be 0: the dW product is not provided */
+  grpo_dtype dtype;
+} grpo_problem;
+
+/*
+ * Workspace bytes needed by grpo_loss_fwd and grpo_loss_bwd for `problem`
+ * on the current device (the chunk plan depends on its SM count).
+ * Either output pointer may be NULL.
+ */
+grpo_status grpo_workspace_size(const grpo_problem *problem, size_t *fwd_bytes,
+                                size_t *bwd_bytes);
+
+/*
+ * Group-relative advantages (aibit.im GRPO blog, GRPO section: several
+ * answers per prompt are scored and an advantage is derived from the rewards
+ * statistically; zjt100.com page, "GRPO 的数学和发现的问题": A is the
+ * advantage after all reward functions). For each group of group_size
+ * contiguous entries: A_b = (r_b - mean) / (std + eps), std with ddof 1 if
+ * std_unbiased else 0; mean and std are formed in float64.
+ *   rewards  device float32 [num_seqs], read only
+ *   adv      device float32 [num_seqs], written
+ * INVALID_ARG if num_seqs < 1, group_size < 1, group_size does not divide
+ * num_seqs, or std_unbiased with group_size < 2.
+ */
+grpo_status grpo_advantages(const float *rewards, int32_t num_seqs, int32_t group_size,
+                            float eps, int32_t std_unbiased, float *adv,
+                            cudaStream_t stream);
+
+/*
+ * Forward pass of the fused loss (zjt100.com page, "Unsloth 高效 GRPO 算法":
+ * a linear-cross-entropy style kernel adapted to GRPO; "GRPO 的数学和发现的问题":
+ * reverse KL, beta, the exp(q - q.detach()) * A term, the logsumexp trick;
+ * Unsloth "grpo-long-context" page: chunk logits kept in float32).
+ * Policy and reference rows share each W tile; per row an online
+ * max / sum-exp over vocab tiles gives the logsumexp, and the target logit
+ * is gathered in the same pass.
+ *   H_pol, H_ref  [N, d] dtype   W [V, d] dtype   ids int32 [N]
+ *   mask uint8 [N] (0 or non-zero)                adv float32 [B]
+ *   logp_pol, logp_ref  float32 [N]  written; 0 at masked rows
+ *   lse_pol             float32 [N]  written; the policy logsumexp, needed by
+ *                                    grpo_loss_bwd; unspecified at masked rows
+ *   loss                float32 [1]  written
+ *   kl_mean             float32 [1]  written (sum mask*KL / sum mask, 0 if no
+ *                                    valid row); may be NULL
+ * Masked rows may carry any id; valid rows need 0 <= id < V (else
+ * GRPO_ERR_BAD_TOKEN on the device).
+ */
+grpo_status grpo_loss_fwd(const grpo_problem *problem, const void *H_pol, const void *H_ref,
+                          const void *W, const int32_t *ids, const uint8_t *mask,
+                          const float *adv, float *logp_pol, float *logp_ref, float *lse_pol,
+                          float *loss, float *kl_mean, void *workspace, size_t workspace_bytes,
+                          cudaStream_t stream);
+
+/*
+ * Backward pass: gradient of `loss` scaled by grad_loss with respect to
+ * H_pol (the reference model is frozen; Unsloth "grpo-long-context" page,
+ * offloaded log-softmax: the backward recomputes the chunked log-softmax).
+ * With c_n = grad_loss * w_n * (A_b + beta * (exp(x_n) - 1)) the logit
+ * gradient is dZ_n = c_n * (softmax(z_n) - onehot(ids_n)) and dH = dZ W.
+ * The logits are recomputed tile by tile for chunks of rows; dZ lives only
+ * as a bf16 chunk in the workspace.
+ *   logp_pol, logp_ref, lse_pol  the outputs of grpo_loss_fwd on the same
+ *                                inputs
+ *   dH      [N, d] dtype, written; rows of masked tokens are 0
+ *   dW      must be NULL (compute_dW = 0)
+ */
+grpo_status grpo_loss_bwd(const grpo_problem *problem, const void *H_pol, const void *W,
+                          const int32_t *ids, const uint8_t *mask, const float *adv,
+                          const float *logp_pol, const float *logp_ref, const float *lse_pol,
+                          float grad_loss, void *dH, float *dW, void *workspace,
+                          size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * Synchronises `stream`, reads and clears the error word of a workspace
+ * used by grpo_loss_fwd or grpo_loss_bwd, and returns GRPO_OK,
+ * GRPO_ERR_TIMEOUT or GRPO_ERR_BAD_TOKEN (timeout wins if both occurred).
+ */
+grpo_status grpo_get_device_status(void *workspace, cudaStream_t stream);
+
+/* Human-readable name of a status code (static string). */
+const char *grpo_status_string(grpo_status status);
+
+/*
+ * Kernel timing, for benchmarks. While enabled, every kernel the library
+ * launches is bracketed by CUDA events recorded on its launching stream.
+ * grpo_profile_collect synchronises on those events and returns, for each
+ * kernel kind k < n_kinds, the summed milliseconds and the launch count
+ * since the last collect (then clears them). Kinds are numbered 0 ..
+ * grpo_profile_kind_count()-1 and named by grpo_profile_kind_name.
+ * Not thread-safe; at most 65536 launches between collects.
+ */
+grpo_status grpo_profile_enable(int32_t on);
+grpo_status grpo_profile_collect(double *ms, int64_t *launches, int32_t n_kinds);
+int32_t grpo_profile_kind_count(void);
+const char *grpo_profile_kind_name(int32_t kind);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GRPO_H */

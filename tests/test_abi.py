@@ -1,0 +1,95 @@
+"""The C-ABI library: it loads, exports every function include/grpo.h
+declares, and rejects malformed problems on the host before touching the
+GPU. No kernel is launched here."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from grpo_loss_gb300 import _lib as L
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared_functions():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", fn)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names |= set(re.findall(r"\b(grpo_[a-z_0-9]+)\s*\(", src))
+    return sorted(names)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(L.LIB_PATH):
+        pytest.skip("library not built (python -m grpo_loss_gb300.build)")
+    return L.lib()
+
+
+def test_header_declares_the_boundary():
+    names = _declared_functions()
+    for required in ("grpo_advantages", "grpo_loss_fwd", "grpo_loss_bwd",
+                     "grpo_workspace_size", "grpo_get_device_status", "grpo_status_string"):
+        assert required in names
+
+
+def test_library_exports_every_declared_function(lib):
+    handle = ctypes.CDLL(L.LIB_PATH)
+    for name in _declared_functions():
+        assert hasattr(handle, name), name
+
+
+def test_status_strings(lib):
+    for code in range(7):
+        assert len(L.status_string(code)) > 1
+    assert L.status_string(99) == "unknown status"
+
+
+def _problem(**kw):
+    base = dict(num_seqs=8, seq_len=64, d=256, V=1024, group_size=4)
+    base.update(kw)
+    p = L.make_problem(**base)
+    return p
+
+
+@pytest.mark.parametrize("field,value,expected", [
+    ("N", 7, 1),                 # N != num_seqs * seq_len
+    ("group_size", 3, 1),        # does not divide num_seqs
+    ("group_size", 0, 1),
+    ("num_seqs", 0, 1),
+    ("d", 4, 1),                 # d < 8
+    ("d", 260, 2),               # d % 8 != 0: rows not 16-byte aligned for TMA
+    ("V", 0, 1),
+    ("chunk_rows", -1, 1),
+    ("compute_dW", 1, 2),
+    ("dtype", 7, 1),
+])
+def test_workspace_size_rejects_bad_problems_on_host(lib, field, value, expected):
+    p = _problem()
+    setattr(p, field, value)
+    f, b = ctypes.c_size_t(0), ctypes.c_size_t(0)
+    assert lib.grpo_workspace_size(ctypes.byref(p), ctypes.byref(f), ctypes.byref(b)) == expected
+
+
+def test_null_problem_and_pointers_rejected(lib):
+    assert lib.grpo_workspace_size(None, None, None) == 1
+    assert lib.grpo_advantages(None, 8, 4, 1e-4, 1, None, None) == 1
+    # unbiased std needs two members per group
+    buf = ctypes.c_void_p(16)
+    assert lib.grpo_advantages(buf, 4, 1, 1e-4, 1, buf, None) == 1
+    p = _problem()
+    args = [ctypes.byref(p)] + [None] * 11 + [None, 0, None]
+    assert lib.grpo_loss_fwd(*args) == 1
+    args = [ctypes.byref(p)] + [None] * 8 + [1.0, None, None, None, 0, None]
+    assert lib.grpo_loss_bwd(*args) == 1
+    assert lib.grpo_get_device_status(None, None) == 1
+
+
+def test_profile_kinds(lib):
+    n = lib.grpo_profile_kind_count()
+    names = [lib.grpo_profile_kind_name(k).decode() for k in range(n)]
+    assert "fwd_gemm_lse" in names and "bwd_dh_gemm" in names and "bwd_dz_gemm" in names
+    assert lib.grpo_profile_kind_name(n).decode() == "unknown"
