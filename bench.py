@@ -1,0 +1,371 @@
+"""Benchmark of the fused GRPO loss (advantages + forward + recompute backward).
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                [--workload NAME]
+
+One step = one pass of the whole path over one batch: group advantages from
+the rewards, grpo_loss_fwd (policy and reference log-probs, KL, loss) and
+grpo_loss_bwd (dH of the policy hidden states), on synthetic inputs shaped
+like the Llama-3.1-8B head at 20K context with 8 generations unless
+--workload says otherwise. Inputs are resident in HBM for `value`; `e2e`
+repeats the step through the public Python API from pinned host buffers
+(host-to-device copies of the step's inputs and the read-back of the loss
+inside the timed region). Under torchrun every rank runs its own replica of
+the workload (weak scaling, no collective on the data path).
+
+--impl reference times the float64 CPU oracle on a bounded sample of rows
+of the same workload (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from grpo_loss_gb300 import workloads as WL  # noqa: E402
+
+METRIC = "GRPO loss fwd+bwd tokens/s at 1 GB300; % of bf16 dense tensor peak"
+DEFAULT_WORKLOAD = WL.LLAMA31_8B_20K.name
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as fh:
+            p = json.load(fh)
+        return {"bf16_tflops": p.get("bf16_tflops"), "bf16_tflops_sustained":
+                p.get("bf16_tflops_sustained"), "hbm_gbs": p.get("hbm_gbs"), "source": "measured"}
+    return {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0,
+            "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples while the timed region runs."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.lines = []
+        self.dev = device_index
+        self.thread = None
+
+    def start(self):
+        try:
+            uuid = str(torch.cuda.get_device_properties(self.dev).uuid)
+            sel = ["-i", "GPU-" + uuid if not uuid.startswith("GPU-") else uuid]
+        except Exception:
+            sel = []
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "--query-gpu=" + self.FIELDS,
+                                          "--format=csv,noheader,nounits", "-lms", "200"] + sel,
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[4:8]):
+                if val.lower().startswith("active"):
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def _flops(w, n_valid):
+    # 2 N d V per logit GEMM: policy + reference forward, policy recompute, dH
+    return {"step": 8.0 * n_valid * w.d * w.V, "fwd_gemm_lse": 4.0 * n_valid * w.d * w.V,
+            "bwd_dz_gemm": 2.0 * n_valid * w.d * w.V, "bwd_dh_gemm": 2.0 * n_valid * w.d * w.V}
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def cpu_oracle_sample(w, inp, rows_target: int = 256, time_budget_s: float = 15.0):
+    """Time the float64 oracle (as it stands) on a bounded sample of valid rows
+    of the workload: both log-prob passes and the backward of those rows."""
+    from oracle import grpo_oracle as O
+    m = inp["mask"].numpy() > 0
+    valid = np.nonzero(m)[0]
+    rng = np.random.default_rng(11)
+    A = (inp["adv"].double().numpy() if w.supplied_adv
+         else O.advantages(inp["rewards"], w.G, w.eps, w.std_unbiased))
+    t0 = time.perf_counter()
+    Wf = O.to_f64(inp["W"])
+    t_conv = time.perf_counter() - t0
+    done, t_rows, n = 0, 0.0, 16
+    while done < rows_target and t_rows < time_budget_s:
+        rows = np.sort(rng.choice(valid, size=min(n, valid.size), replace=False))
+        t1 = time.perf_counter()
+        O.token_logprobs(inp["H_pol"], Wf, inp["ids"], rows=rows)
+        O.token_logprobs(inp["H_ref"], Wf, inp["ids"], rows=rows)
+        O.backward(inp["H_pol"], inp["H_ref"], Wf, inp["ids"], inp["mask"], A, w.B, w.T,
+                   w.beta, rows=rows)
+        t_rows += time.perf_counter() - t1
+        done += rows.size
+        n = min(2 * n, 128)
+    try:
+        from threadpoolctl import threadpool_info
+        cores = max(int(i.get("num_threads", 1)) for i in threadpool_info()) if threadpool_info() else os.cpu_count()
+    except Exception:
+        cores = os.cpu_count()
+    return {"value": done / t_rows, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": "%d valid rows of %s (policy+reference log-probs and backward per row, "
+                      "float64, full vocab), %.1f s; one-off W->float64 conversion %.1f s "
+                      "excluded" % (done, w.name, t_rows, t_conv)}
+
+
+def run_reference(args, w):
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return
+    inp = WL.make_inputs(w)
+    from oracle import grpo_oracle as O
+    m = inp["mask"].numpy() > 0
+    valid = np.nonzero(m)[0]
+    A = (inp["adv"].double().numpy() if w.supplied_adv
+         else O.advantages(inp["rewards"], w.G, w.eps, w.std_unbiased))
+    Wf = O.to_f64(inp["W"])
+    rng = np.random.default_rng(5)
+    rows_per_step = 32 if w.V * w.d > 1e8 else min(valid.size, 512)
+
+    def step():
+        rows = np.sort(rng.choice(valid, size=min(rows_per_step, valid.size), replace=False))
+        O.token_logprobs(inp["H_pol"], Wf, inp["ids"], rows=rows)
+        O.token_logprobs(inp["H_ref"], Wf, inp["ids"], rows=rows)
+        O.backward(inp["H_pol"], inp["H_ref"], Wf, inp["ids"], inp["mask"], A, w.B, w.T,
+                   w.beta, rows=rows)
+        return rows.size
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    rows = sum(step() for _ in range(args.steps))
+    dt = time.perf_counter() - t0
+    value = rows / dt
+    cores = os.cpu_count()
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+            "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * dt / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "tokens_per_step": rows_per_step,
+                       "sample": "rows drawn from the valid tokens"},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                             "sample": "%d valid rows per step of %s, float64 full-vocab oracle"
+                                       % (rows_per_step, w.name)},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, w):
+    import torch.distributed as dist
+
+    import grpo_loss_gb300 as G
+
+    ws, rank, local = _dist()
+    if ws > 1:
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    # every rank runs its own replica of the workload (independent batch)
+    w_r = w if ws == 1 else WL.Workload(**{**w.__dict__, "seed": w.seed + 100 * rank})
+    inp = WL.make_inputs(w_r)
+    n_valid = int(inp["mask"].sum())
+    dt = torch.float32 if w.dtype == "f32" else torch.bfloat16
+
+    eng = G.GRPOLoss(w.B, w.T, w.d, w.V, w.G, beta=w.beta, eps=w.eps,
+                     std_unbiased=w.std_unbiased, dtype=dt, device=dev)
+    d_in = {k: (v.to(dev) if v is not None else None) for k, v in inp.items()}
+    rewards = d_in["rewards"]
+    adv_in = d_in["adv"]
+    dH = torch.empty_like(d_in["H_pol"])
+    stream = torch.cuda.current_stream()
+
+    def step(d):
+        adv = adv_in if w.supplied_adv else eng.advantages(d["rewards"])
+        eng.forward(d["H_pol"], d["H_ref"], d["W"], d["ids"], d["mask"], adv)
+        eng.backward(d["H_pol"], d["W"], d["ids"], d["mask"], adv, 1.0, dH=dH)
+
+    # ---------------------------------------------------------- device-resident
+    for _ in range(args.warmup):
+        step(d_in)
+    torch.cuda.synchronize()
+    eng.check()
+    if ws > 1:
+        dist.barrier()
+    G.profile_enable(True)
+    G.profile_collect()
+    clocks = ClockSampler(local) if rank == 0 else None
+    if clocks:
+        clocks.start()
+        time.sleep(0.3)
+    torch.cuda.synchronize()
+    if ws > 1:
+        dist.barrier()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step(d_in)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    if ws > 1:
+        dist.barrier()
+    clk = clocks.stop() if clocks else None
+    G.profile_enable(False)
+    prof = G.profile_collect()
+    eng.check()
+    ms = ev0.elapsed_time(ev1)
+    t = torch.tensor([ms], dtype=torch.float64, device=dev)
+    if ws > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    ms_max = float(t.item())
+    nv = torch.tensor([n_valid], dtype=torch.float64, device=dev)
+    if ws > 1:
+        dist.all_reduce(nv)
+    total_valid = float(nv.item())
+    ms_step = ms_max / args.steps
+    value = total_valid / (ms_step / 1e3)
+
+    # --------------------------------------------------------------- end to end
+    host = {k: (v.pin_memory() if v is not None else None) for k, v in inp.items()}
+    d_e2e = {k: (torch.empty_like(v, device=dev) if v is not None else None)
+             for k, v in inp.items()}
+    loss_host = torch.empty(2, dtype=torch.float32).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for k, v in host.items() if v is not None)
+    d2h = loss_host.numel() * loss_host.element_size()
+
+    def e2e_step():
+        for k, v in host.items():
+            if v is not None:
+                d_e2e[k].copy_(v, non_blocking=True)
+        step(d_e2e)
+        loss_host[0:1].copy_(eng.loss, non_blocking=True)
+        loss_host[1:2].copy_(eng.kl_mean, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize()
+    if ws > 1:
+        dist.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    et = torch.tensor([e0.elapsed_time(e1)], dtype=torch.float64, device=dev)
+    if ws > 1:
+        dist.all_reduce(et, op=dist.ReduceOp.MAX)
+    e2e_value = total_valid / (float(et.item()) / args.steps / 1e3)
+    eng.check()
+
+    if rank == 0:
+        peaks = _peaks()
+        fl = _flops(w, n_valid)
+        gemms = {k: prof[k] for k in ("fwd_gemm_lse", "bwd_dz_gemm", "bwd_dh_gemm")}
+        dom = max(gemms, key=lambda k: gemms[k][0])
+        dom_ms, dom_launches = gemms[dom]
+        per_launch_flops = fl[dom] * args.steps / dom_launches
+        achieved = per_launch_flops / (dom_ms / dom_launches / 1e3) / 1e12
+        peak = peaks["bf16_tflops_sustained"]
+        launches = int(sum(v[1] for v in prof.values()))
+        kernels = {k: {"ms_per_step": v[0] / args.steps, "launches_per_step": v[1] / args.steps}
+                   for k, v in prof.items() if v[1]}
+        step_tflops = fl["step"] / (ms_step / 1e3) / 1e12
+        cpu = cpu_oracle_sample(w, inp) if ws == 1 and not args.no_cpu_baseline else None
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16" if w.dtype == "bf16" else "f32->bf16", "data": "synthetic",
+            "config": {"workload": w.name, "prompts": w.prompts, "generations": w.G,
+                       "completion_len": w.T, "tokens": w.N, "valid_tokens": n_valid,
+                       "hidden": w.d, "vocab": w.V, "beta": w.beta, "dW": False,
+                       "parallelism": "replicas" if ws > 1 else "single",
+                       "l2": "inputs larger than L2 (H_pol+H_ref+W = %.2f GB)"
+                             % ((inp["H_pol"].numel() * 2 + inp["W"].numel()) *
+                                inp["W"].element_size() / 1e9)},
+            "tflops_per_step": step_tflops,
+            "frac_of_peak": step_tflops / peak,
+            "peak": {"bf16_tflops_sustained": peak, "source": peaks["source"]},
+            "roofline": {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak,
+                         "unit": "TFLOP/s", "frac": achieved / peak, "traffic": None,
+                         "peak_kind": "bf16 sustained (%s)" % peaks["source"]},
+            "kernels": kernels,
+            "gpu_launches": launches,
+            "clocks": clk,
+            "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h},
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
+                    choices=sorted(list(WL.FULL) + list(WL.SMALL)))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    w = WL.FULL.get(args.workload) or WL.SMALL[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_ours(args, w)
+
+
+if __name__ == "__main__":
+    main()

@@ -158,15 +158,18 @@ __global__ void __launch_bounds__(1024) k_block_plan(const uint8_t* __restrict__
 // Merge the vocab-slice partials into each row's logsumexp, form q, p, the
 // KL estimator and the weighted loss terms. Per-CTA float64 partial sums
 // (sum w*A, sum w*KL, sum m*KL) go to `partials` for a fixed-order final sum.
-__device__ __forceinline__ float merge_lse(const float2* p, int n_vs) {
+// Rounding is spelled out (__fmaf_rn, __fadd_rn, __fmul_rn) so that every
+// inlined copy computes bit-identical results: equal policy and reference
+// rows then give exactly x = p - q = 0.
+__device__ __noinline__ float merge_lse(const float2* p, int n_vs) {
   float M = -INFINITY;
   for (int v = 0; v < n_vs; ++v) M = fmaxf(M, p[static_cast<int64_t>(v) * kBM].x);
   float S = 0.f;
   for (int v = 0; v < n_vs; ++v) {
     const float2 e = p[static_cast<int64_t>(v) * kBM];
-    S += e.y * exp2f(e.x - M);
+    S = __fmaf_rn(e.y, exp2f(__fsub_rn(e.x, M)), S);
   }
-  return (M + log2f(S)) * 0.69314718055994531f;
+  return __fmul_rn(__fadd_rn(M, log2f(S)), 0.69314718055994531f);
 }
 
 __global__ void k_fwd_finish(const int* __restrict__ inv, const uint8_t* __restrict__ mask,
@@ -190,12 +193,12 @@ __global__ void k_fwd_finish(const int* __restrict__ inv, const uint8_t* __restr
       ls = merge_lse(pp, n_vs);
       if (mask[n]) {
         const float lse_r = merge_lse(pr, n_vs);
-        const float q = zy[n] - ls;
-        const float p = zy[N + n] - lse_r;
+        const float q = __fsub_rn(zy[n], ls);
+        const float p = __fsub_rn(zy[N + n], lse_r);
         lp = q;
         lr = p;
-        const float x = p - q;
-        const float kl = expm1f(x) - x;
+        const float x = __fsub_rn(p, q);
+        const float kl = __fsub_rn(expm1f(x), x);
         const int b = static_cast<int>(n / T);
         const double w = 1.0 / (static_cast<double>(B) * max(cnt[b], 1));
         sa += w * static_cast<double>(adv[b]);
