@@ -147,6 +147,36 @@ grpo_status grpo_loss_bwd(const grpo_problem *problem, const void *H_pol, const 
                           size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * Forward pass without a workspace, for callers that cannot allocate device
+ * memory: hosts with no allocator of their own, for which cudaMalloc would
+ * synchronise the device, and code running under a memory budget that is
+ * fixed once training starts. This entry point has no counterpart in the
+ * pages; it computes exactly what grpo_loss_fwd computes, with the same
+ * arguments minus the workspace.
+ *
+ * Scratch lives in a static device array of GRPO_NOALLOC_SCRATCH_BYTES that
+ * every GPU loading the library holds until the process exits. Its device
+ * address is looked up on the first call on each device (with that device
+ * current), so make that first call before any stream capture. The call
+ * itself never allocates (no cudaMalloc or cudaFree).
+ *
+ * Every call on a device shares the one array, and the array keeps the last
+ * call's contents: calls that may overlap on the GPU (different streams, or
+ * different host threads) race and must not be issued. Returns
+ * GRPO_ERR_WORKSPACE when the problem needs more scratch than the array
+ * holds (roughly 136 bytes per token for bf16 inputs, so up to about 240K
+ * tokens; float32 inputs also need bf16 copies of H_pol, H_ref and W).
+ * A device-detected error (a valid token id outside [0, V), an expired
+ * pipeline wait) makes *loss NaN, since there is no workspace to query.
+ */
+#define GRPO_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
+grpo_status grpo_loss_fwd_noalloc(const grpo_problem *problem, const void *H_pol,
+                                  const void *H_ref, const void *W, const int32_t *ids,
+                                  const uint8_t *mask, const float *adv, float *logp_pol,
+                                  float *logp_ref, float *lse_pol, float *loss, float *kl_mean,
+                                  cudaStream_t stream);
+
+/*
  * Synchronises `stream`, reads and clears the error word of a workspace
  * used by grpo_loss_fwd or grpo_loss_bwd, and returns GRPO_OK,
  * GRPO_ERR_TIMEOUT or GRPO_ERR_BAD_TOKEN (timeout wins if both occurred).
