@@ -5,7 +5,8 @@ python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
 One step = one pass of the whole path over one batch: group advantages from
 the rewards, grpo_loss_fwd (policy and reference log-probs, KL, loss) and
-grpo_loss_bwd (dH of the policy hidden states), on synthetic inputs shaped
+grpo_loss_bwd (dH of the policy hidden states; with --dW also the lm_head
+gradient dW), on synthetic inputs shaped
 like the Llama-3.1-8B head at 20K context with 8 generations unless
 --workload says otherwise. Inputs are resident in HBM for `value`; `e2e`
 repeats the step through the public Python API from pinned host buffers
@@ -35,6 +36,7 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 from grpo_loss_gb300 import workloads as WL  # noqa: E402
+from grpo_loss_gb300.dist import reduce_timing  # noqa: E402
 
 METRIC = "GRPO loss fwd+bwd tokens/s at 1 GB300; % of bf16 dense tensor peak"
 DEFAULT_WORKLOAD = WL.LLAMA31_8B_20K.name
@@ -113,10 +115,12 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def _flops(w, n_valid):
+def _flops(w, n_valid, dW=False):
     # 2 N d V per logit GEMM: policy + reference forward, policy recompute, dH
-    return {"step": 8.0 * n_valid * w.d * w.V, "fwd_gemm_lse": 4.0 * n_valid * w.d * w.V,
-            "bwd_dz_gemm": 2.0 * n_valid * w.d * w.V, "bwd_dh_gemm": 2.0 * n_valid * w.d * w.V}
+    # (and dW when requested)
+    unit = 2.0 * n_valid * w.d * w.V
+    return {"step": (5.0 if dW else 4.0) * unit, "fwd_gemm_lse": 2.0 * unit,
+            "bwd_dz_gemm": unit, "bwd_dh_gemm": unit, "bwd_dw_gemm": unit}
 
 
 def _dist():
@@ -203,6 +207,11 @@ def run_reference(args, w):
     print(json.dumps(line), flush=True)
 
 
+def replica_workload(w, rank: int):
+    """Rank r's independent batch: the same recipe with its own seed."""
+    return w if rank == 0 else WL.Workload(**{**w.__dict__, "seed": w.seed + 100 * rank})
+
+
 def run_ours(args, w):
     import torch.distributed as dist
 
@@ -213,14 +222,13 @@ def run_ours(args, w):
         dist.init_process_group("nccl")
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    # every rank runs its own replica of the workload (independent batch)
-    w_r = w if ws == 1 else WL.Workload(**{**w.__dict__, "seed": w.seed + 100 * rank})
+    w_r = replica_workload(w, rank)
     inp = WL.make_inputs(w_r)
     n_valid = int(inp["mask"].sum())
     dt = torch.float32 if w.dtype == "f32" else torch.bfloat16
 
     eng = G.GRPOLoss(w.B, w.T, w.d, w.V, w.G, beta=w.beta, eps=w.eps,
-                     std_unbiased=w.std_unbiased, dtype=dt, device=dev)
+                     std_unbiased=w.std_unbiased, dtype=dt, device=dev, compute_dW=args.dW)
     d_in = {k: (v.to(dev) if v is not None else None) for k, v in inp.items()}
     rewards = d_in["rewards"]
     adv_in = d_in["adv"]
@@ -260,15 +268,7 @@ def run_ours(args, w):
     G.profile_enable(False)
     prof = G.profile_collect()
     eng.check()
-    ms = ev0.elapsed_time(ev1)
-    t = torch.tensor([ms], dtype=torch.float64, device=dev)
-    if ws > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    ms_max = float(t.item())
-    nv = torch.tensor([n_valid], dtype=torch.float64, device=dev)
-    if ws > 1:
-        dist.all_reduce(nv)
-    total_valid = float(nv.item())
+    ms_max, total_valid = reduce_timing(ev0.elapsed_time(ev1), n_valid, device=dev)
     ms_step = ms_max / args.steps
     value = total_valid / (ms_step / 1e3)
 
@@ -299,16 +299,15 @@ def run_ours(args, w):
         e2e_step()
     e1.record(stream)
     torch.cuda.synchronize()
-    et = torch.tensor([e0.elapsed_time(e1)], dtype=torch.float64, device=dev)
-    if ws > 1:
-        dist.all_reduce(et, op=dist.ReduceOp.MAX)
-    e2e_value = total_valid / (float(et.item()) / args.steps / 1e3)
+    e2e_ms, _ = reduce_timing(e0.elapsed_time(e1), n_valid, device=dev)
+    e2e_value = total_valid / (e2e_ms / args.steps / 1e3)
     eng.check()
 
     if rank == 0:
         peaks = _peaks()
-        fl = _flops(w, n_valid)
-        gemms = {k: prof[k] for k in ("fwd_gemm_lse", "bwd_dz_gemm", "bwd_dh_gemm")}
+        fl = _flops(w, n_valid, args.dW)
+        gemms = {k: prof[k] for k in ("fwd_gemm_lse", "bwd_dz_gemm", "bwd_dh_gemm",
+                                      "bwd_dw_gemm") if prof[k][1]}
         dom = max(gemms, key=lambda k: gemms[k][0])
         dom_ms, dom_launches = gemms[dom]
         per_launch_flops = fl[dom] * args.steps / dom_launches
@@ -326,7 +325,8 @@ def run_ours(args, w):
             "dtype": "bf16" if w.dtype == "bf16" else "f32->bf16", "data": "synthetic",
             "config": {"workload": w.name, "prompts": w.prompts, "generations": w.G,
                        "completion_len": w.T, "tokens": w.N, "valid_tokens": n_valid,
-                       "hidden": w.d, "vocab": w.V, "beta": w.beta, "dW": False,
+                       "hidden": w.d, "vocab": w.V, "beta": w.beta, "dW": bool(args.dW),
+                       "flops_per_step": fl["step"],
                        "parallelism": "replicas" if ws > 1 else "single",
                        "l2": "inputs larger than L2 (H_pol+H_ref+W = %.2f GB)"
                              % ((inp["H_pol"].numel() * 2 + inp["W"].numel()) *
@@ -359,6 +359,7 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
                     choices=sorted(list(WL.FULL) + list(WL.SMALL)))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--dW", action="store_true", help="also compute the lm_head gradient")
     args = ap.parse_args()
     w = WL.FULL.get(args.workload) or WL.SMALL[args.workload]
     if args.impl == "reference":

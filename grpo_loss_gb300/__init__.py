@@ -23,15 +23,17 @@ class GRPOLoss:
     """Owns the workspaces of one problem shape and runs the library calls.
 
     ``forward`` returns (loss, kl_mean, logp_pol, logp_ref) as CUDA tensors;
-    ``backward`` returns dH_pol. Buffers are allocated once with torch and
+    ``backward`` returns dH_pol (and fills ``self.dW``, float32 [V, d], when
+    built with ``compute_dW``). Buffers are allocated once with torch and
     reused across calls.
     """
 
     def __init__(self, num_seqs: int, seq_len: int, d: int, V: int, group_size: int,
                  beta: float = 0.04, eps: float = 1e-4, std_unbiased: int = 1,
-                 chunk_rows: int = 0, dtype=torch.bfloat16, device="cuda"):
+                 chunk_rows: int = 0, dtype=torch.bfloat16, device="cuda",
+                 compute_dW: bool = False):
         self.problem = make_problem(num_seqs, seq_len, d, V, group_size, beta, eps,
-                                    std_unbiased, chunk_rows, dtype)
+                                    std_unbiased, chunk_rows, dtype, compute_dW)
         fwd_b, bwd_b = workspace_size(self.problem)
         dev = torch.device(device)
         self.ws_fwd = torch.empty(fwd_b, dtype=torch.uint8, device=dev)
@@ -45,6 +47,7 @@ class GRPOLoss:
         self.kl_mean = torch.empty(1, dtype=torch.float32, device=dev)
         self.dtype = dtype
         self.dH = None
+        self.dW = (torch.empty(V, d, dtype=torch.float32, device=dev) if compute_dW else None)
 
     def advantages(self, rewards: torch.Tensor) -> torch.Tensor:
         p = self.problem
@@ -61,7 +64,7 @@ class GRPOLoss:
                 self.dH = torch.empty_like(H_pol)
             dH = self.dH
         loss_bwd(self.problem, H_pol, W, ids, mask, adv, self.logp_pol, self.logp_ref,
-                 self.lse_pol, grad_loss, dH, self.ws_bwd)
+                 self.lse_pol, grad_loss, dH, self.ws_bwd, dW=self.dW)
         return dH
 
     def check(self) -> None:
@@ -85,11 +88,13 @@ class _GRPOLossFn(torch.autograd.Function):
         H_pol, W, ids, mask, adv = ctx.saved_tensors
         # the upstream gradient is read on the host: one scalar per backward
         dH = ctx.engine.backward(H_pol, W, ids, mask, adv, float(g_loss), dH=torch.empty_like(H_pol))
-        return dH, None, None, None, None, None, None
+        dW = ctx.engine.dW.to(W.dtype) if ctx.engine.dW is not None else None
+        return dH, None, dW, None, None, None, None
 
 
 def grpo_loss(H_pol, H_ref, W, ids, mask, adv, engine: GRPOLoss):
     """Autograd entry: returns (loss, kl_mean); backward gives the gradient
-    of the loss with respect to H_pol only (the reference model is frozen;
-    kl_mean is a metric and carries no gradient; dW is not provided)."""
+    of the loss with respect to H_pol, and with respect to W when the engine
+    was built with ``compute_dW`` (the reference model is frozen; kl_mean is a
+    metric and carries no gradient)."""
     return _GRPOLossFn.apply(H_pol, H_ref, W, ids, mask, adv, engine)

@@ -41,10 +41,10 @@ class Problem(ctypes.Structure):
 
 def make_problem(num_seqs: int, seq_len: int, d: int, V: int, group_size: int,
                  beta: float = 0.04, eps: float = 1e-4, std_unbiased: int = 1,
-                 chunk_rows: int = 0, dtype=torch.bfloat16) -> Problem:
+                 chunk_rows: int = 0, dtype=torch.bfloat16, compute_dW: int = 0) -> Problem:
     return Problem(N=num_seqs * seq_len, d=d, V=V, num_seqs=num_seqs, seq_len=seq_len,
                    group_size=group_size, beta=beta, eps=eps, std_unbiased=std_unbiased,
-                   chunk_rows=chunk_rows, compute_dW=0,
+                   chunk_rows=chunk_rows, compute_dW=1 if compute_dW else 0,
                    dtype=GRPO_F32 if dtype == torch.float32 else GRPO_BF16)
 
 
@@ -148,14 +148,15 @@ def loss_fwd(problem: Problem, H_pol, H_ref, W, ids, mask, adv, logp_pol, logp_r
 
 
 def loss_bwd(problem: Problem, H_pol, W, ids, mask, adv, logp_pol, logp_ref, lse_pol,
-             grad_loss: float, dH, workspace: torch.Tensor, stream=None) -> None:
+             grad_loss: float, dH, workspace: torch.Tensor, stream=None, dW=None) -> None:
     N = problem.N
     _check(lib().grpo_loss_bwd(
         ctypes.byref(problem), _ptr(H_pol, "H_pol"), _ptr(W, "W"),
         _ptr(ids, "ids", torch.int32, N), _ptr(mask, "mask", torch.uint8, N),
         _ptr(adv, "adv", torch.float32, problem.num_seqs),
         _ptr(logp_pol, "logp_pol", torch.float32, N), _ptr(logp_ref, "logp_ref", torch.float32, N),
-        _ptr(lse_pol, "lse_pol", torch.float32, N), float(grad_loss), _ptr(dH, "dH"), None,
+        _ptr(lse_pol, "lse_pol", torch.float32, N), float(grad_loss), _ptr(dH, "dH"),
+        _ptr(dW, "dW", torch.float32, problem.V * problem.d),
         _ptr(workspace, "workspace"), workspace.numel() * workspace.element_size(),
         _stream(stream)), "grpo_loss_bwd")
 

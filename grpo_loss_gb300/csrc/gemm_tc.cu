@@ -6,7 +6,12 @@
 //             leave tensor memory.
 //   MODE_DZ   Z = H_pol W^T recomputed for one chunk of rows; the epilogue
 //             writes dZ = c * (softmax(z) - onehot(y)) as bf16.
-//   MODE_DH   dH = dZ W for the same chunk (K = V), stored in H's dtype.
+//   MODE_DH   dH = dZ W for the same chunk (K = V), stored in H's dtype,
+//             with B = W^T [d, V] (K-major; transposed once per call, which
+//             measured faster than reading W MN-major).
+//   MODE_DW   dW += dZ^T H_pol for the same chunk (K = the chunk's tokens);
+//             both operands are read as stored (MN-major), and the fp32
+//             result is accumulated into dW across chunks.
 //
 // One CTA per SM, 6 warps: warp 0 issues TMA loads into a 4-stage shared
 // memory ring, warp 1 owns tensor memory and issues the MMAs, warps 2..5 run
@@ -32,6 +37,14 @@ constexpr int kSmemBytes =
     1024 + kStages * (kAStageBytes + kBStageBytes) + 256;  // alignment slack + ring + barriers
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kGroupBlocks = 16;  // MODE_DZ raster: blocks per group sharing W tiles
+constexpr int kMNBoxBytes = 64 * kBK * 2;  // one 64 (MN) x 64 (K) bf16 TMA box: 8 KB
+
+// Which operands a mode reads MN-major (contiguous along M or N).
+template <int MODE>
+struct Major {
+  static constexpr bool a_mn = MODE == MODE_DW;
+  static constexpr bool b_mn = MODE == MODE_DW;
+};
 
 struct Smem {
   uint64_t full[kStages];
@@ -58,6 +71,7 @@ __device__ __forceinline__ int unit_count(const GemmArgs& g, int nb) {
   if (MODE == MODE_FWD) return 2 * nb * g.n_vs;
   const int nbc = min(g.chunk_nb, nb - g.chunk_b0);
   if (nbc <= 0) return 0;
+  if (MODE == MODE_DW) return g.n_mt * g.n_nt;
   return MODE == MODE_DZ ? nbc * g.n_vt : nbc * g.n_nt;
 }
 
@@ -86,7 +100,7 @@ __device__ __forceinline__ Unit unit_decode(const GemmArgs& g, int nb, int u) {
     r.vs = 0;
     r.row0 = g.blk[g.chunk_b0 + r.jj] * kBM;
     r.a_row = r.row0;
-  } else {
+  } else if (MODE == MODE_DH) {
     r.jj = u / g.n_nt;
     r.t0 = u - r.jj * g.n_nt;
     r.t1 = r.t0 + 1;
@@ -94,6 +108,15 @@ __device__ __forceinline__ Unit unit_decode(const GemmArgs& g, int nb, int u) {
     r.vs = 0;
     r.row0 = g.blk[g.chunk_b0 + r.jj] * kBM;
     r.a_row = r.jj * kBM;  // dZ rows are chunk-local
+  } else {
+    // MODE_DW: output tile (vocab rows mt*128.., hidden columns t*bn..)
+    r.jj = u / g.n_nt;
+    r.t0 = u - r.jj * g.n_nt;
+    r.t1 = r.t0 + 1;
+    r.side = 0;
+    r.vs = 0;
+    r.row0 = r.jj * kBM;
+    r.a_row = r.row0;
   }
   return r;
 }
@@ -142,6 +165,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int nb = *g.nblk_dev;
   const int n_units = unit_count<MODE>(g, nb);
   const uint32_t b_bytes = static_cast<uint32_t>(g.bn) * kBK * 2;
+  // MODE_DW reduces over the chunk's tokens: two 64-row K blocks per block
+  const int nk = MODE == MODE_DW ? 2 * max(0, min(g.chunk_nb, nb - g.chunk_b0)) : g.nk;
+  constexpr bool kAMN = Major<MODE>::a_mn;
+  constexpr bool kBMN = Major<MODE>::b_mn;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -159,14 +186,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         const CUtensorMap* mA = (MODE == MODE_FWD && un.side) ? &mapA1 : &mapA0;
         for (int t = un.t0; ok && t < un.t1; ++t) {
           const int b_row = t * g.bn;
-          for (int kb = 0; kb < g.nk; ++kb) {
+          for (int kb = 0; kb < nk; ++kb) {
             if (!mbar_wait(&sh->empty[s], ph ^ 1u, abort)) {
               ok = false;
               break;
             }
             mbar_arrive_expect_tx(&sh->full[s], kAStageBytes + b_bytes);
-            tma_load_2d(smA + s * kAStageBytes, mA, &sh->full[s], kb * kBK, un.a_row);
-            tma_load_2d(smB + s * kBStageBytes, &mapB, &sh->full[s], kb * kBK, b_row);
+            if (kAMN) {
+              // dZ chunk rows kb*64.. as K, two 64-wide vocab columns as M
+#pragma unroll
+              for (int i = 0; i < kBM / 64; ++i)
+                tma_load_2d(smA + s * kAStageBytes + i * kMNBoxBytes, mA, &sh->full[s],
+                            un.a_row + 64 * i, kb * kBK);
+            } else {
+              tma_load_2d(smA + s * kAStageBytes, mA, &sh->full[s], kb * kBK, un.a_row);
+            }
+            if (kBMN) {
+              // K rows: the chunk's token rows of H (two 64-row halves per block)
+              const int k_row = g.blk[g.chunk_b0 + (kb >> 1)] * kBM + (kb & 1) * 64;
+              for (int i = 0; i < g.bn / 64; ++i)
+                tma_load_2d(smB + s * kBStageBytes + i * kMNBoxBytes, &mapB, &sh->full[s],
+                            b_row + 64 * i, k_row);
+            } else {
+              tma_load_2d(smB + s * kBStageBytes, &mapB, &sh->full[s], kb * kBK, b_row);
+            }
             issued |= 1u << s;
             last_par = (last_par & ~(1u << s)) | (ph << s);
             if (++s == kStages) {
@@ -188,7 +231,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      const uint32_t idesc = idesc_bf16_f32(kBM, static_cast<uint32_t>(g.bn));
+      const uint32_t idesc = idesc_bf16_f32(kBM, static_cast<uint32_t>(g.bn), kAMN, kBMN);
       int s = 0;
       uint32_t ph = 0;
       int ab = 0;
@@ -203,7 +246,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc_fence_after();
           const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(ab * kAccStride);
-          for (int kb = 0; kb < g.nk; ++kb) {
+          for (int kb = 0; kb < nk; ++kb) {
             if (!mbar_wait(&sh->full[s], ph, abort)) {
               ok = false;
               break;
@@ -213,8 +256,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t b_addr = smem_u32(smB + s * kBStageBytes);
 #pragma unroll
             for (int k = 0; k < kBK / 16; ++k) {
-              umma_bf16(d_tmem, sdesc_kmajor_sw128(a_addr + k * 32),
-                        sdesc_kmajor_sw128(b_addr + k * 32), idesc, (kb | k) != 0);
+              // K step of 16: 32 bytes along a K-major row, 16 rows of 128 bytes MN-major
+              const uint64_t ad = kAMN ? sdesc_mnmajor_sw128(a_addr + k * 2048, kMNBoxBytes)
+                                       : sdesc_kmajor_sw128(a_addr + k * 32);
+              const uint64_t bd = kBMN ? sdesc_mnmajor_sw128(b_addr + k * 2048, kMNBoxBytes)
+                                       : sdesc_kmajor_sw128(b_addr + k * 32);
+              umma_bf16(d_tmem, ad, bd, idesc, (kb | k) != 0);
             }
             umma_commit(&sh->empty[s]);
             if (++s == kStages) {
@@ -250,7 +297,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int u = blockIdx.x; ok && u < n_units; u += gridDim.x) {
       const Unit un = unit_decode<MODE>(g, nb, u);
       const int64_t row = static_cast<int64_t>(un.row0) + r_in_tile;
-      const bool in_range = row < g.N;
+      const bool in_range = row < (MODE == MODE_DW ? g.V : g.N);
 
       // per-unit state
       float m2 = -INFINITY, s_run = 0.f, s_comp = 0.f;  // FWD: running max / Kahan sum
@@ -353,6 +400,29 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
             }
           }
+        } else if (MODE == MODE_DW) {
+          const int ncc = g.bn / 32;
+#pragma unroll 1
+          for (int c = 0; c < ncc; ++c) {
+            const int64_t col0 = col_t + c * 32;
+            if (col0 >= g.d) break;  // uniform across the warp
+            uint32_t r[32];
+            tmem_ld32_wait(tbase + c * 32, r);
+            if (in_range) {
+              float4* dst = reinterpret_cast<float4*>(g.dw + row * g.d + col0);
+#pragma unroll
+              for (int v = 0; v < 8; ++v) {
+                if (col0 + 4 * v < g.d) {
+                  float4 a = dst[v];
+                  a.x += __uint_as_float(r[4 * v]);
+                  a.y += __uint_as_float(r[4 * v + 1]);
+                  a.z += __uint_as_float(r[4 * v + 2]);
+                  a.w += __uint_as_float(r[4 * v + 3]);
+                  dst[v] = a;
+                }
+              }
+            }
+          }
         } else {
           const int ncc = g.bn / 32;
 #pragma unroll 1
@@ -428,7 +498,10 @@ cudaError_t gemm_configure() {
   e = cudaFuncSetAttribute(k_gemm<MODE_DZ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            kSmemBytes);
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(k_gemm<MODE_DH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  e = cudaFuncSetAttribute(k_gemm<MODE_DH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kSmemBytes);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(k_gemm<MODE_DW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               kSmemBytes);
 }
 
@@ -439,8 +512,10 @@ cudaError_t launch_gemm(int mode, const CUtensorMap& a0, const CUtensorMap& a1,
     k_gemm<MODE_FWD><<<grid, kThreads, kSmemBytes, stream>>>(a0, a1, b, args);
   else if (mode == MODE_DZ)
     k_gemm<MODE_DZ><<<grid, kThreads, kSmemBytes, stream>>>(a0, a1, b, args);
-  else
+  else if (mode == MODE_DH)
     k_gemm<MODE_DH><<<grid, kThreads, kSmemBytes, stream>>>(a0, a1, b, args);
+  else
+    k_gemm<MODE_DW><<<grid, kThreads, kSmemBytes, stream>>>(a0, a1, b, args);
   return cudaGetLastError();
 }
 

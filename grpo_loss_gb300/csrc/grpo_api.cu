@@ -34,7 +34,8 @@ constexpr size_t kMaxProfiled = 65536;
 
 const char* kKindNames[K_NUM_KINDS] = {
     "advantages", "convert_bf16", "seq_count",  "block_plan",  "fwd_gemm_lse", "fwd_finish",
-    "fwd_reduce", "bwd_coef",     "transpose_w", "zero_rows",  "bwd_dz_gemm",  "bwd_dh_gemm"};
+    "fwd_reduce", "bwd_coef",     "transpose_w", "zero_rows",  "bwd_dz_gemm",  "bwd_dh_gemm",
+    "bwd_dw_gemm"};
 
 void prof_begin(int k, cudaStream_t s) {
   if (!g_prof.on || g_prof.used >= kMaxProfiled) return;
@@ -145,8 +146,10 @@ struct Plan {
   int n_vs;          // forward vocab slices
   int nk_d;          // K blocks over d
   int nk_v;          // K blocks over V
-  int bn_dh;         // dH tile width
-  int n_nt;          // dH column tiles
+  int bn_dh;         // dH and dW tile width (columns of d)
+  int n_nt;          // dH and dW column tiles
+  int n_mt;          // dW row tiles (128 vocab rows)
+  bool dw;           // dW requested
   int chunk_nb;      // blocks per backward chunk
   int n_chunks;
   int64_t ldv;       // padded row length of dZ and W^T
@@ -156,8 +159,6 @@ struct Plan {
   // backward workspace offsets
   size_t b_cnt, b_blk, b_inv, b_coef, b_wt, b_dz, b_hp16, b_w16, b_total;
 };
-
-bool is_pow2ish_tile(int64_t d, int bn) { return d % bn == 0; }
 
 grpo_status validate_problem(const grpo_problem* p) {
   if (!p) return GRPO_ERR_INVALID_ARG;
@@ -171,7 +172,7 @@ grpo_status validate_problem(const grpo_problem* p) {
   if (!isfinite(p->beta) || !isfinite(p->eps)) return GRPO_ERR_INVALID_ARG;
   if (p->dtype != GRPO_F32 && p->dtype != GRPO_BF16) return GRPO_ERR_INVALID_ARG;
   if (p->chunk_rows < 0) return GRPO_ERR_INVALID_ARG;
-  if (p->compute_dW != 0) return GRPO_ERR_UNSUPPORTED;
+  if (p->compute_dW != 0 && p->compute_dW != 1) return GRPO_ERR_INVALID_ARG;
   return GRPO_OK;
 }
 
@@ -206,14 +207,17 @@ grpo_status make_plan(const grpo_problem* p, Plan* pl) {
   P.nk_d = static_cast<int>(ceil_div(P.d, kBK));
   P.nk_v = static_cast<int>(ceil_div(P.V, kBK));
   P.ldv = (P.V + 7) / 8 * 8;
-  // widest dH tile (multiple of 32, <= 256) that divides d; else 256 with a clipped edge
+  // widest tile over d (a multiple of 64, <= 256: dW reads H in 64-column
+  // TMA boxes) that divides d; else 256 with a clipped edge
   P.bn_dh = 256;
-  for (int bn = 256; bn >= 32; bn -= 32)
-    if (is_pow2ish_tile(P.d, bn)) {
+  for (int bn = 256; bn >= 64; bn -= 64)
+    if (P.d % bn == 0) {
       P.bn_dh = bn;
       break;
     }
   P.n_nt = static_cast<int>(ceil_div(P.d, P.bn_dh));
+  P.n_mt = static_cast<int>(ceil_div(P.V, kBM));
+  P.dw = p->compute_dW != 0;
   // backward chunk: rows of the bf16 dZ buffer
   if (p->chunk_rows > 0) {
     P.chunk_nb = static_cast<int>(ceil_div(p->chunk_rows, kBM));
@@ -406,7 +410,8 @@ grpo_status grpo_loss_bwd(const grpo_problem* problem, const void* H_pol, const 
   if (st != GRPO_OK) return st;
   if (!H_pol || !W || !ids || !mask || !adv || !logp_pol || !logp_ref || !lse_pol || !dH)
     return GRPO_ERR_INVALID_ARG;
-  if (dW) return GRPO_ERR_UNSUPPORTED;
+  if ((dW != nullptr) != (problem->compute_dW != 0)) return GRPO_ERR_INVALID_ARG;
+  if (dW && !aligned16(dW)) return GRPO_ERR_UNSUPPORTED;
   if (!isfinite(grad_loss)) return GRPO_ERR_INVALID_ARG;
   Plan P;
   if ((st = make_plan(problem, &P)) != GRPO_OK) return st;
@@ -423,7 +428,6 @@ grpo_status grpo_loss_bwd(const grpo_problem* problem, const void* H_pol, const 
   int* blk = reinterpret_cast<int*>(ws + P.b_blk);
   int* inv = reinterpret_cast<int*>(ws + P.b_inv);
   float* coef = reinterpret_cast<float*>(ws + P.b_coef);
-  __nv_bfloat16* wt = reinterpret_cast<__nv_bfloat16*>(ws + P.b_wt);
   __nv_bfloat16* dz = reinterpret_cast<__nv_bfloat16*>(ws + P.b_dz);
 
   const void* hp = H_pol;
@@ -439,13 +443,19 @@ grpo_status grpo_loss_bwd(const grpo_problem* problem, const void* H_pol, const 
     w = w16;
   }
 
-  CUtensorMap mHp, mW, mDz, mWt;
+  // K-major maps (box 64 x rows) for the recompute and dH; MN-major maps
+  // (box 64 x 64) for dZ and H as dW's operands
+  __nv_bfloat16* wt = reinterpret_cast<__nv_bfloat16*>(ws + P.b_wt);
+  CUtensorMap mHp, mW, mDz, mWt, mDzMn, mHmn;
+  const int64_t dz_rows = static_cast<int64_t>(P.chunk_nb) * kBM;
   if ((st = make_map(&mHp, hp, P.d, P.N, P.d, kBM)) != GRPO_OK) return st;
   if ((st = make_map(&mW, w, P.d, P.V, P.d, kVocabTile)) != GRPO_OK) return st;
-  if ((st = make_map(&mDz, dz, P.V, static_cast<int64_t>(P.chunk_nb) * kBM, P.ldv, kBM)) !=
-      GRPO_OK)
-    return st;
+  if ((st = make_map(&mDz, dz, P.V, dz_rows, P.ldv, kBM)) != GRPO_OK) return st;
   if ((st = make_map(&mWt, wt, P.V, P.d, P.ldv, P.bn_dh)) != GRPO_OK) return st;
+  if (P.dw) {
+    if ((st = make_map(&mDzMn, dz, P.V, dz_rows, P.ldv, 64)) != GRPO_OK) return st;
+    if ((st = make_map(&mHmn, hp, P.d, P.N, P.d, 64)) != GRPO_OK) return st;
+  }
 
   if (cudaMemsetAsync(ctrl, 0, sizeof(Ctrl), stream) != cudaSuccess) return GRPO_ERR_CUDA;
   LAUNCH(K_SEQ_COUNT, stream,
@@ -456,6 +466,8 @@ grpo_status grpo_loss_bwd(const grpo_problem* problem, const void* H_pol, const 
          launch_bwd_coef(mask, cnt, adv, logp_pol, logp_ref, P.N, P.B, P.T, problem->beta,
                          grad_loss, coef, stream));
   LAUNCH(K_TRANSPOSE_W, stream, launch_transpose_w(W, P.f32, P.V, P.d, wt, P.ldv, stream));
+  if (P.dw && cudaMemsetAsync(dW, 0, sizeof(float) * P.V * P.d, stream) != cudaSuccess)
+    return GRPO_ERR_CUDA;
   LAUNCH(K_ZERO_ROWS, stream, launch_zero_invalid_rows(inv, P.N, P.d, dH, P.f32, stream));
 
   GemmArgs g;
@@ -477,11 +489,15 @@ grpo_status grpo_loss_bwd(const grpo_problem* problem, const void* H_pol, const 
   g.ldz = P.ldv;
   g.out = dH;
   g.out_f32 = P.f32 ? 1 : 0;
+  g.dw = dW;
+  g.n_mt = P.n_mt;
   g.err = &ctrl->err;
   const int64_t dz_units = static_cast<int64_t>(P.chunk_nb) * P.n_vt;
   const int64_t dh_units = static_cast<int64_t>(P.chunk_nb) * P.n_nt;
   const int grid_dz = static_cast<int>(dz_units < P.sms ? dz_units : P.sms);
   const int grid_dh = static_cast<int>(dh_units < P.sms ? dh_units : P.sms);
+  const int64_t dw_units = static_cast<int64_t>(P.n_mt) * P.n_nt;
+  const int grid_dw = static_cast<int>(dw_units < P.sms ? dw_units : P.sms);
   for (int c = 0; c < P.n_chunks; ++c) {
     g.chunk_b0 = c * P.chunk_nb;
     GemmArgs gz = g;
@@ -492,6 +508,11 @@ grpo_status grpo_loss_bwd(const grpo_problem* problem, const void* H_pol, const 
     gh.bn = P.bn_dh;
     gh.nk = P.nk_v;
     LAUNCH(K_BWD_DH_GEMM, stream, launch_gemm(MODE_DH, mDz, mDz, mWt, gh, grid_dh, stream));
+    if (P.dw) {
+      GemmArgs gw = g;
+      gw.bn = P.bn_dh;
+      LAUNCH(K_BWD_DW_GEMM, stream, launch_gemm(MODE_DW, mDzMn, mDzMn, mHmn, gw, grid_dw, stream));
+    }
   }
   return GRPO_OK;
 }

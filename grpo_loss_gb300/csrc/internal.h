@@ -16,7 +16,7 @@ constexpr int kBM = 128;         // rows per output tile (one TMEM lane per row)
 constexpr int kBK = 64;          // bf16 K elements per 128-byte swizzled row
 constexpr int kVocabTile = 256;  // vocab columns per tile in the logit GEMMs
 
-enum GemmMode : int { MODE_FWD = 0, MODE_DZ = 1, MODE_DH = 2 };
+enum GemmMode : int { MODE_FWD = 0, MODE_DZ = 1, MODE_DH = 2, MODE_DW = 3 };
 
 // Everything a GEMM launch needs besides its tensor maps.
 struct GemmArgs {
@@ -40,6 +40,8 @@ struct GemmArgs {
   int64_t ldz;
   void* out;              // MODE_DH: dH [N][d]
   int out_f32;
+  float* dw;              // MODE_DW: dW [V][d], accumulated over chunks
+  int n_mt;               // MODE_DW: 128-row vocab tiles
   uint32_t* err;          // device error word
 };
 
@@ -57,6 +59,7 @@ enum KernelKind : int {
   K_ZERO_ROWS,
   K_BWD_DZ_GEMM,
   K_BWD_DH_GEMM,
+  K_BWD_DW_GEMM,
   K_NUM_KINDS
 };
 

@@ -74,7 +74,7 @@ typedef struct grpo_problem {
   float eps;            /* advantage denominator guard, e.g. 1e-4 */
   int32_t std_unbiased; /* 1: group std with Bessel's correction, 0: without */
   int64_t chunk_rows;   /* backward token chunk; 0 = chosen from a 4 GiB dZ budget */
-  int32_t compute_dW;   /* must be 0: the dW product is not provided */
+  int32_t compute_dW;   /* 1: grpo_loss_bwd also writes dW (the lm_head gradient) */
   grpo_dtype dtype;
 } grpo_problem;
 
@@ -134,11 +134,15 @@ grpo_status grpo_loss_fwd(const grpo_problem *problem, const void *H_pol, const 
  * With c_n = grad_loss * w_n * (A_b + beta * (exp(x_n) - 1)) the logit
  * gradient is dZ_n = c_n * (softmax(z_n) - onehot(ids_n)) and dH = dZ W.
  * The logits are recomputed tile by tile for chunks of rows; dZ lives only
- * as a bf16 chunk in the workspace.
+ * as a bf16 chunk in the workspace. With compute_dW the same chunk also
+ * feeds dW = sum over chunks of dZ^T H_pol (a full fine-tune trains the
+ * lm_head; LoRA and QLoRA runs freeze it, hence optional).
  *   logp_pol, logp_ref, lse_pol  the outputs of grpo_loss_fwd on the same
  *                                inputs
  *   dH      [N, d] dtype, written; rows of masked tokens are 0
- *   dW      must be NULL (compute_dW = 0)
+ *   dW      float32 [V, d], written (accumulated in float32 over chunks in a
+ *           fixed order), required when compute_dW = 1 and NULL otherwise
+ *           (else GRPO_ERR_INVALID_ARG)
  */
 grpo_status grpo_loss_bwd(const grpo_problem *problem, const void *H_pol, const void *W,
                           const int32_t *ids, const uint8_t *mask, const float *adv,

@@ -26,13 +26,13 @@ def oracle_adv(w: WL.Workload, inp) -> np.ndarray:
 
 def gpu_run(w: WL.Workload, inp, adv32: torch.Tensor, chunk_rows: int = 0, beta=None,
             grad: float = 1.0, H_ref=None, ids=None, mask=None, want_bwd: bool = True,
-            check: bool = True):
+            check: bool = True, want_dW: bool = False):
     """Forward (+ backward) through the library; returns host tensors."""
     import grpo_loss_gb300 as G
     dev = torch.device("cuda")
     eng = G.GRPOLoss(w.B, w.T, w.d, w.V, w.G, beta=w.beta if beta is None else beta,
                      eps=w.eps, std_unbiased=w.std_unbiased, chunk_rows=chunk_rows,
-                     dtype=torch_dtype(w), device=dev)
+                     dtype=torch_dtype(w), device=dev, compute_dW=want_dW)
     Hp = inp["H_pol"].to(dev)
     Hr = (inp["H_ref"] if H_ref is None else H_ref).to(dev)
     Wd = inp["W"].to(dev)
@@ -44,6 +44,8 @@ def gpu_run(w: WL.Workload, inp, adv32: torch.Tensor, chunk_rows: int = 0, beta=
     if want_bwd:
         dH = eng.backward(Hp, Wd, idd, md, adv, grad)
         out["dH"] = dH.float().cpu()
+        if want_dW:
+            out["dW"] = eng.dW.cpu()
     torch.cuda.synchronize()
     if check:
         eng.check()

@@ -64,7 +64,7 @@ def _problem(**kw):
     ("d", 260, 2),               # d % 8 != 0: rows not 16-byte aligned for TMA
     ("V", 0, 1),
     ("chunk_rows", -1, 1),
-    ("compute_dW", 1, 2),
+    ("compute_dW", 2, 1),
     ("dtype", 7, 1),
 ])
 def test_workspace_size_rejects_bad_problems_on_host(lib, field, value, expected):

@@ -63,6 +63,42 @@ def test_forward_backward_match_oracle(w):
     _compare(w, res, f, g, inp["mask"])
 
 
+@pytest.mark.parametrize("w,chunk_rows", [(WL.TINY, 0), (WL.SMALL["qwen2.5-small"], 256),
+                                          (WL.SMALL["gpt-oss-small"], 0),
+                                          (WL.SMALL["qwen3-small"], 128)],
+                         ids=["tiny", "qwen2.5-small-chunk256", "gpt-oss-small",
+                              "qwen3-small-chunk128"])
+def test_dW_matches_oracle(w, chunk_rows):
+    """dW = sum over chunks of dZ^T H_pol, with several chunks accumulating."""
+    inp = WL.make_inputs(w)
+    adv32 = torch.from_numpy(oracle_adv(w, inp)).float()
+    res = gpu_run(w, inp, adv32, chunk_rows=chunk_rows, want_dW=True)
+    g = O.backward(inp["H_pol"], inp["H_ref"], inp["W"], inp["ids"], inp["mask"],
+                   adv32.double(), w.B, w.T, w.beta, want_dW=True)
+    assert rel_l2(res["dW"].numpy(), g["dW"]) < TOL_DH_L2, rel_l2(res["dW"].numpy(), g["dW"])
+    assert rel_l2(res["dH"].numpy(), g["dH"]) < TOL_DH_L2
+
+
+def test_dW_ragged_and_rejected_without_flag():
+    import grpo_loss_gb300 as G
+    w = WL.Workload("ragged-dw", prompts=1, G=3, T=50, d=200, V=1001, mask="pad_uniform",
+                    pad_lo=25, pad_hi=50, rewards="normal", seed=78)
+    inp = WL.make_inputs(w)
+    adv32 = torch.from_numpy(oracle_adv(w, inp)).float()
+    res = gpu_run(w, inp, adv32, chunk_rows=128, want_dW=True)
+    g = O.backward(inp["H_pol"], inp["H_ref"], inp["W"], inp["ids"], inp["mask"],
+                   adv32.double(), w.B, w.T, w.beta, want_dW=True)
+    assert rel_l2(res["dW"].numpy(), g["dW"]) < TOL_DH_L2
+    # dW pointer without compute_dW (and the reverse) is an argument error
+    eng = res["engine"]
+    with pytest.raises(G.GrpoError) as e:
+        G.loss_bwd(eng.problem, inp["H_pol"].cuda(), inp["W"].cuda(), inp["ids"].cuda(),
+                   inp["mask"].cuda(), adv32.cuda(), eng.logp_pol, eng.logp_ref, eng.lse_pol,
+                   1.0, torch.empty(w.N, w.d, dtype=torch.bfloat16, device="cuda"), eng.ws_bwd,
+                   dW=None)
+    assert e.value.status == 1
+
+
 def test_small_chunks_give_identical_gradients_and_runs_are_deterministic():
     w = WL.SMALL["qwen2.5-small"]
     inp = WL.make_inputs(w)
