@@ -53,6 +53,42 @@ def _peaks():
             "source": "fallback"}
 
 
+def kernel_source_hash() -> str:
+    """sha256 over the library's CUDA/C++ sources and its public header: a
+    DRAM traffic figure measured on other sources no longer applies."""
+    import glob
+    import hashlib
+    h = hashlib.sha256()
+    files = sorted(glob.glob(os.path.join(ROOT, "grpo_loss_gb300", "csrc", "*")))
+    files.append(os.path.join(ROOT, "include", "grpo.h"))
+    for f in files:
+        h.update(os.path.basename(f).encode())
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def measured_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum)
+    of `kernel` on `workload`, from the ncu summary in profiles/, or None when
+    there is none or it was taken on different kernel sources."""
+    path = os.path.join(ROOT, "profiles", "traffic_%s_%s.txt" % (kernel, workload))
+    if not os.path.exists(path):
+        return None
+    kv = {}
+    with open(path) as fh:
+        for line in fh:
+            if ":" in line and not line.startswith("#"):
+                k, v = line.split(":", 1)
+                kv[k.strip()] = v.strip()
+    if kv.get("source_sha256") != kernel_source_hash():
+        return None
+    try:
+        return float(kv["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
 class ClockSampler:
     """nvidia-smi clock / throttle-reason samples while the timed region runs."""
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -335,7 +371,8 @@ def run_ours(args, w):
             "frac_of_peak": step_tflops / peak,
             "peak": {"bf16_tflops_sustained": peak, "source": peaks["source"]},
             "roofline": {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak,
-                         "unit": "TFLOP/s", "frac": achieved / peak, "traffic": None,
+                         "unit": "TFLOP/s", "frac": achieved / peak,
+                         "traffic": measured_traffic(dom, w.name),
                          "peak_kind": "bf16 sustained (%s)" % peaks["source"]},
             "kernels": kernels,
             "gpu_launches": launches,

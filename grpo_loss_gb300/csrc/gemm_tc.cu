@@ -36,7 +36,6 @@ constexpr int kAccStride = 256;  // TMEM columns per accumulator buffer
 constexpr int kSmemBytes =
     1024 + kStages * (kAStageBytes + kBStageBytes) + 256;  // alignment slack + ring + barriers
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr int kGroupBlocks = 16;  // MODE_DZ raster: blocks per group sharing W tiles
 constexpr int kMNBoxBytes = 64 * kBK * 2;  // one 64 (MN) x 64 (K) bf16 TMA box: 8 KB
 
 // Which operands a mode reads MN-major (contiguous along M or N).
@@ -89,11 +88,13 @@ __device__ __forceinline__ Unit unit_decode(const GemmArgs& g, int nb, int u) {
     r.t1 = static_cast<int>((static_cast<int64_t>(r.vs + 1) * g.n_vt) / g.n_vs);
   } else if (MODE == MODE_DZ) {
     const int nbc = min(g.chunk_nb, nb - g.chunk_b0);
-    const int gsz_full = kGroupBlocks * g.n_vt;
+    // groups of g.group_blocks blocks walk the vocab tiles together, so each
+    // W tile is fetched once per group while the group's A blocks stay in L2
+    const int gsz_full = g.group_blocks * g.n_vt;
     const int grp = u / gsz_full;
-    const int gb = min(kGroupBlocks, nbc - grp * kGroupBlocks);
+    const int gb = min(g.group_blocks, nbc - grp * g.group_blocks);
     const int rem = u - grp * gsz_full;
-    r.jj = grp * kGroupBlocks + rem % gb;
+    r.jj = grp * g.group_blocks + rem % gb;
     r.t0 = rem / gb;
     r.t1 = r.t0 + 1;
     r.side = 0;

@@ -17,6 +17,7 @@ constexpr size_t kAlign = 256;
 constexpr uint64_t kDefaultDzBudget = 4ull << 30;  // bytes of the bf16 dZ chunk
 constexpr int kFinishGrid = 608;                   // CTAs of the per-token finish kernel
 constexpr int kMaxSlices = 8;                      // vocab slices per block in the forward
+constexpr double kL2ABudget = 40e6;                // bytes of A blocks kept resident in L2
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -203,7 +204,30 @@ grpo_status make_plan(const grpo_problem* p, Plan* pl) {
   P.f32 = p->dtype == GRPO_F32;
   P.nblk_max = static_cast<int>(ceil_div(P.N, kBM));
   P.n_vt = static_cast<int>(ceil_div(P.V, kVocabTile));
-  P.n_vs = P.n_vt < kMaxSlices ? P.n_vt : kMaxSlices;
+  // Forward vocab slices. Units (side, block, slice) run slice-fastest, so
+  // about sms / n_vs blocks are resident at once and share each W tile; keep
+  // their A blocks (128 x d bf16 each) within ~40 MB of L2, and add slices
+  // only when that evens out the last wave of units noticeably.
+  {
+    const double a_blk = 2.0 * kBM * static_cast<double>(P.d);
+    int cb = static_cast<int>(kL2ABudget / a_blk);
+    if (cb < 1) cb = 1;
+    int vmin = static_cast<int>(ceil_div(sms, cb));
+    const int vmax = P.n_vt < kMaxSlices ? P.n_vt : kMaxSlices;
+    if (vmin > vmax) vmin = vmax;
+    if (vmin < 1) vmin = 1;
+    auto wave_eff = [&](int v) {
+      const double waves = 2.0 * P.nblk_max * v / sms;
+      return waves / ceil(waves);
+    };
+    P.n_vs = vmin;
+    double best = wave_eff(vmin);
+    for (int v = vmin + 1; v <= vmax; ++v)
+      if (wave_eff(v) > best + 0.03) {
+        best = wave_eff(v);
+        P.n_vs = v;
+      }
+  }
   P.nk_d = static_cast<int>(ceil_div(P.d, kBK));
   P.nk_v = static_cast<int>(ceil_div(P.V, kBK));
   P.ldv = (P.V + 7) / 8 * 8;
@@ -478,6 +502,7 @@ grpo_status grpo_loss_bwd(const grpo_problem* problem, const void* H_pol, const 
   g.n_vs = 1;
   g.n_nt = P.n_nt;
   g.chunk_nb = P.chunk_nb;
+  g.group_blocks = P.sms / 4 > 16 ? P.sms / 4 : 16;
   g.nblk_max = P.nblk_max;
   g.N = P.N;
   g.d = P.d;

@@ -29,6 +29,7 @@ struct GemmArgs {
   int nk;                 // 64-wide K blocks
   int chunk_b0;           // MODE_DZ/DH: first compacted block of the chunk
   int chunk_nb;           // MODE_DZ/DH: blocks per chunk
+  int group_blocks;       // MODE_DZ: blocks per raster group
   int nblk_max;           // ceil(N / 128)
   int64_t N, d, V;
   const int32_t* ids;

@@ -168,8 +168,10 @@ grpo_status grpo_loss_bwd(const grpo_problem *problem, const void *H_pol, const 
  * call's contents: calls that may overlap on the GPU (different streams, or
  * different host threads) race and must not be issued. Returns
  * GRPO_ERR_WORKSPACE when the problem needs more scratch than the array
- * holds (roughly 136 bytes per token for bf16 inputs, so up to about 240K
- * tokens; float32 inputs also need bf16 copies of H_pol, H_ref and W).
+ * holds (grpo_workspace_size gives the forward's need: for bf16 inputs
+ * 8 + 16 * S bytes per token with S = 1..8 vocab slices, e.g. 72 bytes on
+ * the Llama-8B head, so a few hundred thousand tokens fit; float32 inputs
+ * also need bf16 copies of H_pol, H_ref and W).
  * A device-detected error (a valid token id outside [0, V), an expired
  * pipeline wait) makes *loss NaN, since there is no workspace to query.
  */

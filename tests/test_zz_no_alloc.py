@@ -109,8 +109,8 @@ def test_noalloc_matches_regular_forward_on_two_calls_in_a_row():
 
 def test_noalloc_rejects_problems_beyond_its_scratch():
     fn = _noalloc_fn()
-    w = WL.GPTOSS_20B                                     # ~36 MB of scratch > 32 MiB
-    p = _problem(w)
+    # 64 sequences of 32K tokens on the Llama-8B head: far beyond 32 MiB of scratch
+    p = L.make_problem(64, 32768, 4096, 128256, 8)
     fwd_bytes, _ = L.workspace_size(p)
     assert fwd_bytes > (32 << 20)
     z = torch.zeros(1, device="cuda")
