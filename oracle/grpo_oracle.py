@@ -37,6 +37,22 @@ materialised in float64:
   "grpo-long-context" page (offloaded log-softmax section) changes where the
   logits come from, not this value.
 
+Optional variants, all off by default:
+
+* Logit transforms, in the order of the arguments of the pages' chunked
+  selective log-softmax (Unsloth "grpo-long-context" page, flattened
+  sequence chunking: logit_scale_multiply, logit_scale_divide,
+  logit_softcapping, temperature; item 3: softcapping and temperature are
+  supported): z <- z * multiply / divide, then z <- cap * tanh(z / cap),
+  then z <- z / temperature, before the log-softmax. The pages fix no order;
+  this is the order of the arguments.
+* Token-level aggregation: the loss is sum_n m_n l_n / sum_n m_n instead of
+  the per-sequence mean averaged over sequences (the pages are silent on the
+  aggregation; this is the other common GRPO normalisation).
+* Reference log-probabilities supplied by the caller instead of computed
+  from H_ref (the reference model is frozen, so its log-probs can come from
+  elsewhere, e.g. generation time).
+
 All inputs are taken at their exact values (bf16 and float32 upcast exactly to
 float64). Functions that take ``rows`` compute the listed rows only; every
 per-row quantity depends on that row alone, apart from the per-sequence
@@ -50,7 +66,7 @@ import numpy as np
 
 __all__ = [
     "to_f64", "advantages", "sequence_weights", "token_logprobs", "kl_estimator",
-    "forward", "loss_coefficients", "backward", "logit_memory_gib",
+    "forward", "loss_coefficients", "backward", "logit_memory_gib", "transform_logits",
     "hidden_state_memory_gib",
 ]
 
@@ -86,22 +102,55 @@ def advantages(rewards, group_size: int, eps: float, std_unbiased: int = 1) -> n
     return ((g - mean) / (np.sqrt(var) + eps)).reshape(B)
 
 
-def sequence_weights(mask, num_seqs: int, seq_len: int):
-    """Per-token weights w_n = m_n / (B * max(cnt_b, 1)) and counts cnt_b.
+def sequence_weights(mask, num_seqs: int, seq_len: int, token_level: bool = False):
+    """Per-token weights and the per-sequence counts cnt_b.
 
-    A sequence with no valid token contributes nothing but still counts in B.
+    Default: w_n = m_n / (B * max(cnt_b, 1)); a sequence with no valid token
+    contributes nothing but still counts in B. Token level:
+    w_n = m_n / max(sum_n m_n, 1).
     """
     m = to_f64(mask).reshape(num_seqs, seq_len)
     cnt = m.sum(axis=1)
-    w = m / (num_seqs * np.maximum(cnt, 1.0))[:, None]
+    if token_level:
+        w = m / max(m.sum(), 1.0)
+    else:
+        w = m / (num_seqs * np.maximum(cnt, 1.0))[:, None]
     return w.reshape(-1), cnt
 
 
-def token_logprobs(H, W, ids, rows: Optional[Sequence[int]] = None, row_block: int = 256):
-    """log softmax(H W^T)[n, ids[n]] and the row logsumexp, float64.
+def transform_logits(Z, xform=None):
+    """(z', dz'/dz) for the optional logit transforms.
+
+    ``xform`` maps any of "multiply", "divide", "softcap", "temperature" to a
+    value; a missing key or 0 leaves that step out. Steps in order:
+    z * multiply / divide, cap * tanh(z / cap), z / temperature.
+    """
+    Z = np.asarray(Z, np.float64)
+    if not xform:
+        return Z, np.ones_like(Z)
+    g = 1.0
+    mul = xform.get("multiply") or 1.0
+    div = xform.get("divide") or 1.0
+    cap = xform.get("softcap") or 0.0
+    temp = xform.get("temperature") or 1.0
+    Zt = Z * (mul / div)
+    g = np.full_like(Z, mul / div)
+    if cap:
+        th = np.tanh(Zt / cap)
+        Zt = cap * th
+        g = g * (1.0 - th * th)
+    Zt = Zt / temp
+    g = g / temp
+    return Zt, g
+
+
+def token_logprobs(H, W, ids, rows: Optional[Sequence[int]] = None, row_block: int = 256,
+                   xform=None):
+    """log softmax(f(H W^T))[n, ids[n]] and the row logsumexp, float64.
 
     The full vocab row of logits is formed for every row (in blocks of
-    ``row_block`` rows to bound memory); lse = max + log(sum(exp(z - max))).
+    ``row_block`` rows to bound memory), f is ``transform_logits`` (the
+    identity by default); lse = max + log(sum(exp(z - max))).
     Returns (logp [R], lse [R]) for the requested rows (all rows by default).
     """
     Hs = H if rows is None else H[np.asarray(rows)]
@@ -117,7 +166,7 @@ def token_logprobs(H, W, ids, rows: Optional[Sequence[int]] = None, row_block: i
     lse = np.empty(R)
     for r0 in range(0, R, row_block):
         r1 = min(R, r0 + row_block)
-        Z = Hf[r0:r1] @ Wf.T
+        Z, _ = transform_logits(Hf[r0:r1] @ Wf.T, xform)
         zmax = Z.max(axis=1)
         s = np.exp(Z - zmax[:, None]).sum(axis=1)
         lse[r0:r1] = zmax + np.log(s)
@@ -133,24 +182,29 @@ def kl_estimator(logp_pol, logp_ref) -> np.ndarray:
 
 
 def forward(H_pol, H_ref, W, ids, mask, adv, num_seqs: int, seq_len: int,
-            beta: float) -> Dict[str, np.ndarray]:
+            beta: float, token_level: bool = False, xform=None,
+            logp_ref_given=None) -> Dict[str, np.ndarray]:
     """The GRPO loss forward pass over all N = num_seqs * seq_len tokens.
 
     Returns logp_pol, logp_ref, lse_pol (per token; log-probs are 0 at
     masked tokens), kl (0 at masked tokens), weights w, loss and kl_mean
-    (masked mean of KL; 0 when no token is valid).
+    (masked mean of KL; 0 when no token is valid). With ``logp_ref_given``
+    the reference log-probs are taken from it and H_ref is not used.
     """
     m = to_f64(mask).reshape(-1)
     A = to_f64(adv).reshape(-1)
     # masked tokens may carry any id (e.g. a padding label); score id 0 there
     ids_safe = np.where(m > 0, np.asarray(to_f64(ids), dtype=np.int64).reshape(-1), 0)
     Wf = to_f64(W)
-    q, lse_q = token_logprobs(H_pol, Wf, ids_safe)
-    p, _ = token_logprobs(H_ref, Wf, ids_safe)
+    q, lse_q = token_logprobs(H_pol, Wf, ids_safe, xform=xform)
+    if logp_ref_given is None:
+        p, _ = token_logprobs(H_ref, Wf, ids_safe, xform=xform)
+    else:
+        p = to_f64(logp_ref_given).reshape(-1)
     q = np.where(m > 0, q, 0.0)
     p = np.where(m > 0, p, 0.0)
     kl = np.where(m > 0, kl_estimator(q, p), 0.0)
-    w, cnt = sequence_weights(m, num_seqs, seq_len)
+    w, cnt = sequence_weights(m, num_seqs, seq_len, token_level)
     A_tok = np.repeat(A, seq_len)
     # exp(q - q.detach()) has value 1, so the per-token loss is -(A - beta KL)
     ell = -(A_tok - beta * kl)
@@ -173,12 +227,14 @@ def loss_coefficients(logp_pol, logp_ref, adv_tok, w, beta: float, grad_loss: fl
 
 def backward(H_pol, H_ref, W, ids, mask, adv, num_seqs: int, seq_len: int, beta: float,
              grad_loss: float = 1.0, rows: Optional[Sequence[int]] = None,
-             want_dW: bool = False, want_dZ: bool = False, row_block: int = 256):
+             want_dW: bool = False, want_dZ: bool = False, row_block: int = 256,
+             token_level: bool = False, xform=None, logp_ref_given=None):
     """Gradients of the loss: dH_pol (rows requested, or all) and optionally dW.
 
     Per row: q and p from ``token_logprobs`` (the reference rows are needed
-    for x = p - q), c_n from ``loss_coefficients``, then
-    dZ_n = c_n * (softmax(z_n) - onehot(ids_n)), dH_n = dZ_n W and
+    for x = p - q, unless ``logp_ref_given``), c_n from
+    ``loss_coefficients``, then, with z' = f(z) the transformed logits,
+    dZ_n = c_n * (softmax(z'_n) - onehot(ids_n)) * f'(z_n), dH_n = dZ_n W and
     dW = sum_n dZ_n^T H_pol[n]. Masked rows have c = 0.
     ``want_dW`` requires all rows.
     """
@@ -188,9 +244,10 @@ def backward(H_pol, H_ref, W, ids, mask, adv, num_seqs: int, seq_len: int, beta:
     rows_arr = np.arange(N) if rows is None else np.asarray(rows, dtype=np.int64)
     if want_dW and rows is not None:
         raise ValueError("dW needs every row")
-    w, _ = sequence_weights(m, num_seqs, seq_len)
+    w, _ = sequence_weights(m, num_seqs, seq_len, token_level)
     Wf = to_f64(W)
     V, d = Wf.shape
+    p_given = None if logp_ref_given is None else to_f64(logp_ref_given).reshape(-1)
     ids_all = np.asarray(to_f64(ids), dtype=np.int64).reshape(-1)
     dH = np.zeros((rows_arr.size, d))
     dW = np.zeros((V, d)) if want_dW else None
@@ -199,13 +256,18 @@ def backward(H_pol, H_ref, W, ids, mask, adv, num_seqs: int, seq_len: int, beta:
         rr = rows_arr[r0:r0 + row_block]
         valid = m[rr] > 0
         Hp = to_f64(H_pol[rr])
-        Z = Hp @ Wf.T
+        Z, fprime = transform_logits(Hp @ Wf.T, xform)
         zmax = Z.max(axis=1)
         lse = zmax + np.log(np.exp(Z - zmax[:, None]).sum(axis=1))
         sel = ids_all[rr]
         safe = np.where(valid, sel, 0)
         q = Z[np.arange(rr.size), safe] - lse
-        p, _ = token_logprobs(H_ref, Wf, ids_all, rows=rr[valid]) if valid.any() else (np.zeros(0), None)
+        if p_given is not None:
+            p = p_given[rr[valid]]
+        elif valid.any():
+            p, _ = token_logprobs(H_ref, Wf, ids_all, rows=rr[valid], xform=xform)
+        else:
+            p = np.zeros(0)
         p_full = np.zeros(rr.size)
         p_full[valid] = p
         c = loss_coefficients(q, p_full, A[rr // seq_len], w[rr], beta, grad_loss)
@@ -213,6 +275,7 @@ def backward(H_pol, H_ref, W, ids, mask, adv, num_seqs: int, seq_len: int, beta:
         dZ = np.exp(Z - lse[:, None])
         dZ[np.arange(rr.size), safe] -= 1.0
         dZ *= c[:, None]
+        dZ *= fprime
         dH[r0:r0 + rr.size] = dZ @ Wf
         if want_dW:
             dW += dZ.T @ Hp

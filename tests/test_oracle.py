@@ -250,3 +250,125 @@ def test_memory_model_against_printed_figures():
         val = O.logit_memory_gib(int(r), int(v), int(mult), int(bpe))
         assert abs(val - float(printed)) <= float(tol), (name.strip(), val, printed)
     assert abs(O.hidden_state_memory_gib(8, 64000, 4096) - 1.953125) < 1e-12
+
+
+# ------------------------------------------------------ optional variants
+
+XF = {"multiply": 1.5, "divide": 1.2, "softcap": 3.0, "temperature": 0.7}
+
+
+def test_scale_and_temperature_equal_scaled_weights():
+    H, W = _rand((40, 10), 31), _rand((90, 10), 32, 0.7)
+    ids = np.arange(40) % 90
+    for xf, factor in [({"multiply": 2.0}, 2.0), ({"divide": 4.0}, 0.25),
+                       ({"temperature": 2.0}, 0.5), ({"multiply": 3.0, "divide": 2.0,
+                                                      "temperature": 0.5}, 3.0)]:
+        a, la = O.token_logprobs(H, W, ids, xform=xf)
+        b, lb = O.token_logprobs(H, factor * W, ids)
+        assert np.allclose(a, b, rtol=1e-13, atol=1e-13) and np.allclose(la, lb, rtol=1e-13)
+
+
+def test_softcap_bounds_and_large_cap_limit():
+    H, W = _rand((30, 8), 33, 3.0), _rand((50, 8), 34, 2.0)
+    Z, g = O.transform_logits((H @ W.T).numpy(), {"softcap": 5.0})
+    assert np.all(np.abs(Z) < 5.0) and np.all((g > 0) & (g <= 1.0))
+    ids = np.arange(30)
+    a, _ = O.token_logprobs(H, W, ids, xform={"softcap": 1e7})
+    b, _ = O.token_logprobs(H, W, ids)
+    assert np.allclose(a, b, rtol=1e-9, atol=1e-9)
+
+
+def test_transform_matches_torch_literal_log_softmax():
+    H, W = _rand((60, 12), 35), _rand((80, 12), 36, 0.6)
+    ids = torch.randint(0, 80, (60,), generator=torch.Generator().manual_seed(7))
+    z = (H @ W.T) * XF["multiply"] / XF["divide"]
+    z = XF["softcap"] * torch.tanh(z / XF["softcap"]) / XF["temperature"]
+    ref = torch.log_softmax(z, dim=1)[torch.arange(60), ids]
+    a, _ = O.token_logprobs(H, W, ids, xform=XF)
+    assert np.allclose(a, ref.numpy(), rtol=1e-13, atol=1e-12)
+
+
+def _literal_torch_loss_v(P, H, W, token_level=False, xform=None):
+    B, T = P["B"], P["T"]
+
+    def f(z):
+        if not xform:
+            return z
+        z = z * xform["multiply"] / xform["divide"]
+        z = xform["softcap"] * torch.tanh(z / xform["softcap"])
+        return z / xform["temperature"]
+
+    q = torch.log_softmax(f(H @ W.T), dim=1)[torch.arange(B * T), P["ids"]]
+    with torch.no_grad():
+        p = torch.log_softmax(f(P["Hr"] @ W.detach().T), dim=1)[torch.arange(B * T), P["ids"]]
+    A = torch.from_numpy(np.repeat(P["A"], T))
+    m = P["mask"].double()
+    obj = torch.exp(q - q.detach()) * A - P["beta"] * (torch.exp(p - q) - (p - q) - 1)
+    if token_level:
+        return -(obj * m).sum() / m.sum().clamp(min=1)
+    per_seq = (obj * m).reshape(B, T).sum(1) / m.reshape(B, T).sum(1).clamp(min=1)
+    return -per_seq.mean()
+
+
+@pytest.mark.parametrize("token_level,xform", [(True, None), (False, XF), (True, XF)],
+                         ids=["token-level", "transforms", "both"])
+def test_variants_match_literal_autograd(token_level, xform):
+    P = _problem()
+    H = P["Hp"].clone().requires_grad_(True)
+    W = P["W"].clone().requires_grad_(True)
+    L = _literal_torch_loss_v(P, H, W, token_level, xform)
+    L.backward()
+    f = O.forward(P["Hp"], P["Hr"], P["W"], P["ids"], P["mask"], P["A"], P["B"], P["T"],
+                  P["beta"], token_level=token_level, xform=xform)
+    assert abs(f["loss"] - L.item()) < 1e-14
+    b = O.backward(P["Hp"], P["Hr"], P["W"], P["ids"], P["mask"], P["A"], P["B"], P["T"],
+                   P["beta"], want_dW=True, token_level=token_level, xform=xform)
+    assert np.allclose(b["dH"], H.grad.numpy(), rtol=1e-10, atol=1e-16)
+    assert np.allclose(b["dW"], W.grad.numpy(), rtol=1e-10, atol=1e-16)
+
+
+def test_finite_differences_with_softcap_and_token_level():
+    P = _problem(B=4, T=4, G=2, d=8, V=32, seed=22, scale=1.2)
+    xf = {"softcap": 2.0, "temperature": 0.8}
+    w, _ = O.sequence_weights(P["mask"], P["B"], P["T"], token_level=True)
+    At = np.repeat(P["A"], P["T"])
+    m = P["mask"].numpy() > 0
+    Hp, Hr, W = P["Hp"].numpy(), P["Hr"].numpy(), P["W"].numpy()
+    ids = P["ids"].numpy()
+
+    def Ls(Hp_):
+        q, _ = O.token_logprobs(Hp_, W, ids, xform=xf)
+        p, _ = O.token_logprobs(Hr, W, ids, xform=xf)
+        return float(np.sum(np.where(m, w * (-At * q + P["beta"] * O.kl_estimator(q, p)), 0.0)))
+
+    b = O.backward(Hp, Hr, W, ids, P["mask"], P["A"], P["B"], P["T"], P["beta"],
+                   token_level=True, xform=xf)
+    h = 1e-6
+    rng = np.random.default_rng(1)
+    for (i, j) in [tuple(rng.integers(0, s) for s in Hp.shape) for _ in range(12)]:
+        Hplus, Hminus = Hp.copy(), Hp.copy()
+        Hplus[i, j] += h
+        Hminus[i, j] -= h
+        fd = (Ls(Hplus) - Ls(Hminus)) / (2 * h)
+        assert abs(fd - b["dH"][i, j]) <= 1e-7 * max(1.0, abs(b["dH"][i, j])) + 1e-9
+
+
+def test_token_level_reference_equal_policy():
+    P = _problem()
+    f = O.forward(P["Hp"], P["Hp"], P["W"], P["ids"], P["mask"], P["A"], P["B"], P["T"],
+                  P["beta"], token_level=True)
+    m = P["mask"].numpy().reshape(P["B"], P["T"]).astype(float)
+    expected = -np.sum(m.sum(1) * P["A"]) / m.sum()
+    assert abs(f["loss"] - expected) < 1e-15 and f["kl_mean"] == 0.0
+
+
+def test_given_reference_logprobs_equal_computed_ones():
+    P = _problem()
+    f = O.forward(P["Hp"], P["Hr"], P["W"], P["ids"], P["mask"], P["A"], P["B"], P["T"], P["beta"])
+    g = O.forward(P["Hp"], None, P["W"], P["ids"], P["mask"], P["A"], P["B"], P["T"], P["beta"],
+                  logp_ref_given=f["logp_ref"])
+    assert g["loss"] == f["loss"] and np.array_equal(g["kl"], f["kl"])
+    b1 = O.backward(P["Hp"], P["Hr"], P["W"], P["ids"], P["mask"], P["A"], P["B"], P["T"], P["beta"])
+    b2 = O.backward(P["Hp"], None, P["W"], P["ids"], P["mask"], P["A"], P["B"], P["T"], P["beta"],
+                    logp_ref_given=f["logp_ref"])
+    assert np.allclose(b1["dH"], b2["dH"], rtol=1e-14, atol=1e-18)
