@@ -31,9 +31,13 @@ class GRPOLoss:
     def __init__(self, num_seqs: int, seq_len: int, d: int, V: int, group_size: int,
                  beta: float = 0.04, eps: float = 1e-4, std_unbiased: int = 1,
                  chunk_rows: int = 0, dtype=torch.bfloat16, device="cuda",
-                 compute_dW: bool = False):
+                 compute_dW: bool = False, token_level: bool = False,
+                 logit_multiply: float = 0.0, logit_divide: float = 0.0, softcap: float = 0.0,
+                 temperature: float = 0.0, ref_logp_given: bool = False):
         self.problem = make_problem(num_seqs, seq_len, d, V, group_size, beta, eps,
-                                    std_unbiased, chunk_rows, dtype, compute_dW)
+                                    std_unbiased, chunk_rows, dtype, compute_dW, token_level,
+                                    logit_multiply, logit_divide, softcap, temperature,
+                                    ref_logp_given)
         fwd_b, bwd_b = workspace_size(self.problem)
         dev = torch.device(device)
         self.ws_fwd = torch.empty(fwd_b, dtype=torch.uint8, device=dev)
@@ -53,7 +57,13 @@ class GRPOLoss:
         p = self.problem
         return advantages(rewards, p.group_size, p.eps, p.std_unbiased, self.adv)
 
-    def forward(self, H_pol, H_ref, W, ids, mask, adv):
+    def forward(self, H_pol, H_ref, W, ids, mask, adv, logp_ref=None):
+        """With ``ref_logp_given`` pass H_ref=None and the reference log-probs
+        as ``logp_ref`` (float32 [N]); they are copied into the engine."""
+        if self.problem.ref_logp_given:
+            if logp_ref is None:
+                raise ValueError("ref_logp_given needs logp_ref")
+            self.logp_ref.copy_(logp_ref)
         loss_fwd(self.problem, H_pol, H_ref, W, ids, mask, adv, self.logp_pol, self.logp_ref,
                  self.lse_pol, self.loss, self.kl_mean, self.ws_fwd)
         return self.loss, self.kl_mean, self.logp_pol, self.logp_ref

@@ -36,16 +36,25 @@ class Problem(ctypes.Structure):
                 ("group_size", ctypes.c_int32), ("beta", ctypes.c_float),
                 ("eps", ctypes.c_float), ("std_unbiased", ctypes.c_int32),
                 ("chunk_rows", ctypes.c_int64), ("compute_dW", ctypes.c_int32),
-                ("dtype", ctypes.c_int32)]
+                ("dtype", ctypes.c_int32), ("token_level", ctypes.c_int32),
+                ("logit_multiply", ctypes.c_float), ("logit_divide", ctypes.c_float),
+                ("softcap", ctypes.c_float), ("temperature", ctypes.c_float),
+                ("ref_logp_given", ctypes.c_int32)]
 
 
 def make_problem(num_seqs: int, seq_len: int, d: int, V: int, group_size: int,
                  beta: float = 0.04, eps: float = 1e-4, std_unbiased: int = 1,
-                 chunk_rows: int = 0, dtype=torch.bfloat16, compute_dW: int = 0) -> Problem:
+                 chunk_rows: int = 0, dtype=torch.bfloat16, compute_dW: int = 0,
+                 token_level: bool = False, logit_multiply: float = 0.0,
+                 logit_divide: float = 0.0, softcap: float = 0.0, temperature: float = 0.0,
+                 ref_logp_given: bool = False) -> Problem:
     return Problem(N=num_seqs * seq_len, d=d, V=V, num_seqs=num_seqs, seq_len=seq_len,
                    group_size=group_size, beta=beta, eps=eps, std_unbiased=std_unbiased,
                    chunk_rows=chunk_rows, compute_dW=1 if compute_dW else 0,
-                   dtype=GRPO_F32 if dtype == torch.float32 else GRPO_BF16)
+                   dtype=GRPO_F32 if dtype == torch.float32 else GRPO_BF16,
+                   token_level=1 if token_level else 0, logit_multiply=logit_multiply,
+                   logit_divide=logit_divide, softcap=softcap, temperature=temperature,
+                   ref_logp_given=1 if ref_logp_given else 0)
 
 
 _lib = None
@@ -138,7 +147,8 @@ def loss_fwd(problem: Problem, H_pol, H_ref, W, ids, mask, adv, logp_pol, logp_r
              loss, kl_mean, workspace: torch.Tensor, stream=None) -> None:
     N = problem.N
     _check(lib().grpo_loss_fwd(
-        ctypes.byref(problem), _ptr(H_pol, "H_pol"), _ptr(H_ref, "H_ref"), _ptr(W, "W"),
+        ctypes.byref(problem), _ptr(H_pol, "H_pol"),
+        None if H_ref is None else _ptr(H_ref, "H_ref"), _ptr(W, "W"),
         _ptr(ids, "ids", torch.int32, N), _ptr(mask, "mask", torch.uint8, N),
         _ptr(adv, "adv", torch.float32, problem.num_seqs),
         _ptr(logp_pol, "logp_pol", torch.float32, N), _ptr(logp_ref, "logp_ref", torch.float32, N),

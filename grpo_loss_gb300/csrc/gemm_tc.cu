@@ -67,7 +67,7 @@ struct Unit {
 
 template <int MODE>
 __device__ __forceinline__ int unit_count(const GemmArgs& g, int nb) {
-  if (MODE == MODE_FWD) return 2 * nb * g.n_vs;
+  if (MODE == MODE_FWD) return g.n_sides * nb * g.n_vs;
   const int nbc = min(g.chunk_nb, nb - g.chunk_b0);
   if (nbc <= 0) return 0;
   if (MODE == MODE_DW) return g.n_mt * g.n_nt;
@@ -124,6 +124,20 @@ __device__ __forceinline__ Unit unit_decode(const GemmArgs& g, int nb, int u) {
 
 __device__ __forceinline__ void set_error(uint32_t* err, uint32_t bit) {
   if (err) atomicOr(err, bit);
+}
+
+// Optional logit transform z' = f(z): scale, then softcap, then temperature;
+// also returns f'(z) for the backward.
+__device__ __forceinline__ float xform_logit(const GemmArgs& g, float z, float* fprime) {
+  float u = z * g.x_scale;
+  float gr = g.x_scale;
+  if (g.x_cap > 0.f) {
+    const float th = tanh_via_exp(u / g.x_cap);
+    u = g.x_cap * th;
+    gr *= 1.f - th * th;
+  }
+  *fprime = gr * g.x_inv_temp;
+  return u * g.x_inv_temp;
 }
 
 template <int MODE>
@@ -334,6 +348,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int c = 0; c < kVocabTile / 32; ++c) {
             uint32_t r[32];
             tmem_ld32_wait(tbase + c * 32, r);
+            if (g.xform) {  // uniform across the grid
+              float fp;
+#pragma unroll
+              for (int j = 0; j < 32; ++j)
+                r[j] = __float_as_uint(xform_logit(g, __uint_as_float(r[j]), &fp));
+            }
             const int64_t col0 = col_t + c * 32;
             float z[32];
             float cm = -INFINITY;
@@ -381,14 +401,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t r[32];
             tmem_ld32_wait(tbase + c * 32, r);
             float o[32];
-#pragma unroll
-            for (int j = 0; j < 32; ++j)
-              o[j] = live ? c_n * ex2_approx(fmaf(__uint_as_float(r[j]), kLog2e, -lse2)) : 0.f;
-            const int64_t off = static_cast<int64_t>(y) - col0;
-            if (off >= 0 && off < 32) {
+            if (!g.xform) {
 #pragma unroll
               for (int j = 0; j < 32; ++j)
-                if (j == off) o[j] -= c_n;
+                o[j] = live ? c_n * ex2_approx(fmaf(__uint_as_float(r[j]), kLog2e, -lse2)) : 0.f;
+              const int64_t off = static_cast<int64_t>(y) - col0;
+              if (off >= 0 && off < 32) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                  if (j == off) o[j] -= c_n;
+              }
+            } else {
+              // dZ = c (softmax(z') - onehot) f'(z) with z' = f(z)
+              const int64_t off = static_cast<int64_t>(y) - col0;
+#pragma unroll
+              for (int j = 0; j < 32; ++j) {
+                float fp;
+                const float zt = xform_logit(g, __uint_as_float(r[j]), &fp);
+                const float sm = ex2_approx(fmaf(zt, kLog2e, -lse2)) - (j == off ? 1.f : 0.f);
+                o[j] = live ? c_n * sm * fp : 0.f;
+              }
             }
             uint32_t pk[16];
 #pragma unroll

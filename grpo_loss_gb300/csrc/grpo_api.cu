@@ -174,6 +174,10 @@ grpo_status validate_problem(const grpo_problem* p) {
   if (p->dtype != GRPO_F32 && p->dtype != GRPO_BF16) return GRPO_ERR_INVALID_ARG;
   if (p->chunk_rows < 0) return GRPO_ERR_INVALID_ARG;
   if (p->compute_dW != 0 && p->compute_dW != 1) return GRPO_ERR_INVALID_ARG;
+  if (p->token_level != 0 && p->token_level != 1) return GRPO_ERR_INVALID_ARG;
+  if (p->ref_logp_given != 0 && p->ref_logp_given != 1) return GRPO_ERR_INVALID_ARG;
+  for (float v : {p->logit_multiply, p->logit_divide, p->softcap, p->temperature})
+    if (!isfinite(v) || v < 0.f) return GRPO_ERR_INVALID_ARG;
   return GRPO_OK;
 }
 
@@ -294,6 +298,17 @@ grpo_status make_plan(const grpo_problem* p, Plan* pl) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
+// Logit transform parameters of a problem (0 in a field means "off").
+void set_xform(const grpo_problem* p, GemmArgs* g) {
+  const float mul = p->logit_multiply > 0.f ? p->logit_multiply : 1.f;
+  const float div = p->logit_divide > 0.f ? p->logit_divide : 1.f;
+  const float temp = p->temperature > 0.f ? p->temperature : 1.f;
+  g->x_scale = mul / div;
+  g->x_cap = p->softcap;
+  g->x_inv_temp = 1.f / temp;
+  g->xform = (g->x_scale != 1.f || g->x_cap > 0.f || g->x_inv_temp != 1.f) ? 1 : 0;
+}
+
 // Control block at the start of every workspace.
 struct Ctrl {
   uint32_t err;
@@ -346,9 +361,11 @@ grpo_status grpo_loss_fwd(const grpo_problem* problem, const void* H_pol, const 
                           cudaStream_t stream) {
   grpo_status st = validate_problem(problem);
   if (st != GRPO_OK) return st;
-  if (!H_pol || !H_ref || !W || !ids || !mask || !adv || !logp_pol || !logp_ref || !lse_pol ||
-      !loss)
+  const bool ref_given = problem->ref_logp_given != 0;
+  if (!H_pol || (!H_ref && !ref_given) || !W || !ids || !mask || !adv || !logp_pol ||
+      !logp_ref || !lse_pol || !loss)
     return GRPO_ERR_INVALID_ARG;
+  if (ref_given) H_ref = H_pol;  // not read: only policy units are launched
   Plan P;
   if ((st = make_plan(problem, &P)) != GRPO_OK) return st;
   if (!aligned16(H_pol) || !aligned16(H_ref) || !aligned16(W)) return GRPO_ERR_UNSUPPORTED;
@@ -412,16 +429,19 @@ grpo_status grpo_loss_fwd(const grpo_problem* problem, const void* H_pol, const 
   g.zy = zy;
   g.part = part;
   g.err = &ctrl->err;
-  const int64_t units = 2ll * P.nblk_max * P.n_vs;
+  g.n_sides = ref_given ? 1 : 2;
+  set_xform(problem, &g);
+  const int64_t units = static_cast<int64_t>(g.n_sides) * P.nblk_max * P.n_vs;
   const int grid = static_cast<int>(units < P.sms ? units : P.sms);
   LAUNCH(K_FWD_GEMM, stream, launch_gemm(MODE_FWD, mHp, mHr, mW, g, grid, stream));
 
   LAUNCH(K_FWD_FINISH, stream,
          launch_fwd_finish(inv, mask, cnt, adv, zy, part, P.nblk_max, P.n_vs, P.N, P.B, P.T,
-                           logp_pol, logp_ref, lse_pol, partials, kFinishGrid, stream));
+                           problem->token_level, ref_given ? 1 : 0, logp_pol, logp_ref,
+                           lse_pol, partials, kFinishGrid, stream));
   LAUNCH(K_FWD_REDUCE, stream,
-         launch_fwd_reduce(partials, kFinishGrid, cnt, P.B, problem->beta, loss,
-                           kl_mean ? kl_mean : &ctrl->kl_scratch, stream));
+         launch_fwd_reduce(partials, kFinishGrid, cnt, P.B, problem->beta, problem->token_level,
+                           loss, kl_mean ? kl_mean : &ctrl->kl_scratch, stream));
   return GRPO_OK;
 }
 
@@ -488,7 +508,7 @@ grpo_status grpo_loss_bwd(const grpo_problem* problem, const void* H_pol, const 
          launch_block_plan(mask, P.N, P.nblk_max, blk, inv, &ctrl->nblk, stream));
   LAUNCH(K_BWD_COEF, stream,
          launch_bwd_coef(mask, cnt, adv, logp_pol, logp_ref, P.N, P.B, P.T, problem->beta,
-                         grad_loss, coef, stream));
+                         grad_loss, problem->token_level, coef, stream));
   LAUNCH(K_TRANSPOSE_W, stream, launch_transpose_w(W, P.f32, P.V, P.d, wt, P.ldv, stream));
   if (P.dw && cudaMemsetAsync(dW, 0, sizeof(float) * P.V * P.d, stream) != cudaSuccess)
     return GRPO_ERR_CUDA;
@@ -517,6 +537,7 @@ grpo_status grpo_loss_bwd(const grpo_problem* problem, const void* H_pol, const 
   g.dw = dW;
   g.n_mt = P.n_mt;
   g.err = &ctrl->err;
+  set_xform(problem, &g);
   const int64_t dz_units = static_cast<int64_t>(P.chunk_nb) * P.n_vt;
   const int64_t dh_units = static_cast<int64_t>(P.chunk_nb) * P.n_nt;
   const int grid_dz = static_cast<int>(dz_units < P.sms ? dz_units : P.sms);

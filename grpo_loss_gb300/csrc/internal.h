@@ -41,6 +41,11 @@ struct GemmArgs {
   int64_t ldz;
   void* out;              // MODE_DH: dH [N][d]
   int out_f32;
+  int n_sides;            // MODE_FWD: 2 (policy and reference) or 1 (policy only)
+  int xform;              // logit transform on (MODE_FWD, MODE_DZ)
+  float x_scale;          // logit_multiply / logit_divide
+  float x_cap;            // softcap (0 = off)
+  float x_inv_temp;       // 1 / temperature
   float* dw;              // MODE_DW: dW [V][d], accumulated over chunks
   int n_mt;               // MODE_DW: 128-row vocab tiles
   uint32_t* err;          // device error word
@@ -82,14 +87,16 @@ cudaError_t launch_block_plan(const uint8_t* mask, int64_t N, int nblk, int* blk
                               int* nblk_dev, cudaStream_t s);
 cudaError_t launch_fwd_finish(const int* inv, const uint8_t* mask, const int* cnt,
                               const float* adv, const float* zy, const float2* part,
-                              int nblk_max, int n_vs, int64_t N, int B, int T, float* logp_pol,
-                              float* logp_ref, float* lse_pol, double* partials, int grid,
-                              cudaStream_t s);
+                              int nblk_max, int n_vs, int64_t N, int B, int T, int token_level,
+                              int ref_given, float* logp_pol, float* logp_ref, float* lse_pol,
+                              double* partials, int grid, cudaStream_t s);
 cudaError_t launch_fwd_reduce(const double* partials, int nparts, const int* cnt, int B,
-                              float beta, float* loss, float* kl_mean, cudaStream_t s);
+                              float beta, int token_level, float* loss, float* kl_mean,
+                              cudaStream_t s);
 cudaError_t launch_bwd_coef(const uint8_t* mask, const int* cnt, const float* adv,
                             const float* logp_pol, const float* logp_ref, int64_t N, int B,
-                            int T, float beta, float grad, float* coef, cudaStream_t s);
+                            int T, float beta, float grad, int token_level, float* coef,
+                            cudaStream_t s);
 cudaError_t launch_transpose_w(const void* W, int w_f32, int64_t V, int64_t d,
                                __nv_bfloat16* Wt, int64_t ldwt, cudaStream_t s);
 cudaError_t launch_zero_invalid_rows(const int* inv, int64_t N, int64_t d, void* out,

@@ -185,6 +185,15 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
+// tanh from the identity tanh(x) = sign(x) * (1 - 2 / (exp(2|x|) + 1)),
+// with 2^x from ex2_approx; absolute error ~1e-7 (relative error grows as
+// |x| -> 0, where the value itself is tiny).
+__device__ __forceinline__ float tanh_via_exp(float x) {
+  const float e = ex2_approx(2.0f * 1.4426950408889634f * fabsf(x));
+  const float t = 1.0f - __fdividef(2.0f, e + 1.0f);
+  return copysignf(t, x);
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));

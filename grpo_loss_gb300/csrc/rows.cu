@@ -172,12 +172,16 @@ __device__ __noinline__ float merge_lse(const float2* p, int n_vs) {
   return __fmul_rn(__fadd_rn(M, log2f(S)), 0.69314718055994531f);
 }
 
+// token_level: the weights are 1 here and the final sum is divided by the
+// number of valid tokens. ref_given: p is read from logp_ref (and logp_ref is
+// not written).
 __global__ void k_fwd_finish(const int* __restrict__ inv, const uint8_t* __restrict__ mask,
                              const int* __restrict__ cnt, const float* __restrict__ adv,
                              const float* __restrict__ zy, const float2* __restrict__ part,
-                             int nblk_max, int n_vs, int64_t N, int B, int T,
-                             float* __restrict__ logp_pol, float* __restrict__ logp_ref,
-                             float* __restrict__ lse_pol, double* __restrict__ partials) {
+                             int nblk_max, int n_vs, int64_t N, int B, int T, int token_level,
+                             int ref_given, float* __restrict__ logp_pol,
+                             float* __restrict__ logp_ref, float* __restrict__ lse_pol,
+                             double* __restrict__ partials) {
   __shared__ double red[3][32];
   double sa = 0.0, sk = 0.0, sm = 0.0;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
@@ -192,22 +196,22 @@ __global__ void k_fwd_finish(const int* __restrict__ inv, const uint8_t* __restr
       const float2* pr = part + ((static_cast<int64_t>(nblk_max) + j) * n_vs) * kBM + r;
       ls = merge_lse(pp, n_vs);
       if (mask[n]) {
-        const float lse_r = merge_lse(pr, n_vs);
         const float q = __fsub_rn(zy[n], ls);
-        const float p = __fsub_rn(zy[N + n], lse_r);
+        const float p = ref_given ? logp_ref[n] : __fsub_rn(zy[N + n], merge_lse(pr, n_vs));
         lp = q;
         lr = p;
         const float x = __fsub_rn(p, q);
         const float kl = __fsub_rn(expm1f(x), x);
         const int b = static_cast<int>(n / T);
-        const double w = 1.0 / (static_cast<double>(B) * max(cnt[b], 1));
+        const double w =
+            token_level ? 1.0 : 1.0 / (static_cast<double>(B) * max(cnt[b], 1));
         sa += w * static_cast<double>(adv[b]);
         sk += w * static_cast<double>(kl);
         sm += static_cast<double>(kl);
       }
     }
     logp_pol[n] = lp;
-    logp_ref[n] = lr;
+    if (!ref_given) logp_ref[n] = lr;
     lse_pol[n] = ls;
   }
   sa = warp_sum_d(sa);
@@ -238,8 +242,8 @@ __global__ void k_fwd_finish(const int* __restrict__ inv, const uint8_t* __restr
 
 // Single warp: fixed-order sum of the per-CTA partials.
 __global__ void k_fwd_reduce(const double* __restrict__ partials, int nparts,
-                             const int* __restrict__ cnt, int B, float beta, float* loss,
-                             float* kl_mean) {
+                             const int* __restrict__ cnt, int B, float beta, int token_level,
+                             float* loss, float* kl_mean) {
   const int lane = threadIdx.x;
   double a = 0.0, k = 0.0, m = 0.0, c = 0.0;
   for (int i = lane; i < nparts; i += 32) {
@@ -253,24 +257,41 @@ __global__ void k_fwd_reduce(const double* __restrict__ partials, int nparts,
   m = warp_sum_d(m);
   c = warp_sum_d(c);
   if (lane == 0) {
-    *loss = static_cast<float>(-a + static_cast<double>(beta) * k);
+    const double l = -a + static_cast<double>(beta) * k;
+    *loss = static_cast<float>(token_level ? l / (c > 1.0 ? c : 1.0) : l);
     if (kl_mean) *kl_mean = c > 0.0 ? static_cast<float>(m / c) : 0.f;
   }
 }
 
 // -------------------------------------------------------- bwd coefficient
 // c_n = g * w_n * (A_b + beta * (exp(p - q) - 1)) at valid rows, 0 elsewhere.
+// Token level: w_n = 1 / max(sum_b cnt_b, 1), the total formed per CTA.
 __global__ void k_bwd_coef(const uint8_t* __restrict__ mask, const int* __restrict__ cnt,
                            const float* __restrict__ adv, const float* __restrict__ logp_pol,
                            const float* __restrict__ logp_ref, int64_t N, int B, int T,
-                           float beta, float grad, float* __restrict__ coef) {
+                           float beta, float grad, int token_level,
+                           float* __restrict__ coef) {
+  __shared__ int64_t s_tot[32];
+  double w_tok = 0.0;
+  if (token_level) {
+    int64_t t = 0;
+    for (int i = threadIdx.x; i < B; i += blockDim.x) t += cnt[i];
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+    if ((threadIdx.x & 31) == 0) s_tot[threadIdx.x >> 5] = t;
+    __syncthreads();
+    int64_t tot = 0;
+    for (int i = 0; i < static_cast<int>(blockDim.x >> 5); ++i) tot += s_tot[i];
+    w_tok = 1.0 / static_cast<double>(tot > 1 ? tot : 1);
+  }
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   for (int64_t n = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; n < N;
        n += stride) {
     float c = 0.f;
     if (mask[n]) {
       const int b = static_cast<int>(n / T);
-      const double w = 1.0 / (static_cast<double>(B) * max(cnt[b], 1));
+      const double w =
+          token_level ? w_tok : 1.0 / (static_cast<double>(B) * max(cnt[b], 1));
       const float x = logp_ref[n] - logp_pol[n];
       c = static_cast<float>(static_cast<double>(grad) * w *
                              (static_cast<double>(adv[b]) +
@@ -352,26 +373,29 @@ cudaError_t launch_block_plan(const uint8_t* mask, int64_t N, int nblk, int* blk
 
 cudaError_t launch_fwd_finish(const int* inv, const uint8_t* mask, const int* cnt,
                               const float* adv, const float* zy, const float2* part,
-                              int nblk_max, int n_vs, int64_t N, int B, int T, float* logp_pol,
-                              float* logp_ref, float* lse_pol, double* partials, int grid,
-                              cudaStream_t s) {
+                              int nblk_max, int n_vs, int64_t N, int B, int T, int token_level,
+                              int ref_given, float* logp_pol, float* logp_ref, float* lse_pol,
+                              double* partials, int grid, cudaStream_t s) {
   k_fwd_finish<<<grid, 256, 0, s>>>(inv, mask, cnt, adv, zy, part, nblk_max, n_vs, N, B, T,
-                                    logp_pol, logp_ref, lse_pol, partials);
+                                    token_level, ref_given, logp_pol, logp_ref, lse_pol,
+                                    partials);
   return cudaGetLastError();
 }
 
 cudaError_t launch_fwd_reduce(const double* partials, int nparts, const int* cnt, int B,
-                              float beta, float* loss, float* kl_mean, cudaStream_t s) {
-  k_fwd_reduce<<<1, 32, 0, s>>>(partials, nparts, cnt, B, beta, loss, kl_mean);
+                              float beta, int token_level, float* loss, float* kl_mean,
+                              cudaStream_t s) {
+  k_fwd_reduce<<<1, 32, 0, s>>>(partials, nparts, cnt, B, beta, token_level, loss, kl_mean);
   return cudaGetLastError();
 }
 
 cudaError_t launch_bwd_coef(const uint8_t* mask, const int* cnt, const float* adv,
                             const float* logp_pol, const float* logp_ref, int64_t N, int B,
-                            int T, float beta, float grad, float* coef, cudaStream_t s) {
+                            int T, float beta, float grad, int token_level, float* coef,
+                            cudaStream_t s) {
   const int blocks = static_cast<int>(std::min<int64_t>((N + 255) / 256, 4096));
   k_bwd_coef<<<blocks, 256, 0, s>>>(mask, cnt, adv, logp_pol, logp_ref, N, B, T, beta, grad,
-                                    coef);
+                                    token_level, coef);
   return cudaGetLastError();
 }
 

@@ -76,6 +76,19 @@ typedef struct grpo_problem {
   int64_t chunk_rows;   /* backward token chunk; 0 = chosen from a 4 GiB dZ budget */
   int32_t compute_dW;   /* 1: grpo_loss_bwd also writes dW (the lm_head gradient) */
   grpo_dtype dtype;
+  /* Optional variants; a zero-initialised field keeps the default. */
+  int32_t token_level;  /* 1: loss = sum_n m_n l_n / sum_n m_n (token-level mean)
+                           instead of the per-sequence mean averaged over B */
+  float logit_multiply; /* logit transforms, applied in this order before the
+                           log-softmax (Unsloth "grpo-long-context" page: the
+                           chunked selective log-softmax takes logit scale,
+                           softcapping and temperature): z *= logit_multiply */
+  float logit_divide;   /*   z /= logit_divide                (0 = off)      */
+  float softcap;        /*   z = softcap * tanh(z / softcap)  (0 = off)      */
+  float temperature;    /*   z /= temperature                 (0 = off)      */
+  int32_t ref_logp_given; /* 1: grpo_loss_fwd reads the reference log-probs
+                             from logp_ref instead of computing them; H_ref
+                             is not used and may be NULL */
 } grpo_problem;
 
 /*
@@ -112,7 +125,9 @@ grpo_status grpo_advantages(const float *rewards, int32_t num_seqs, int32_t grou
  * is gathered in the same pass.
  *   H_pol, H_ref  [N, d] dtype   W [V, d] dtype   ids int32 [N]
  *   mask uint8 [N] (0 or non-zero)                adv float32 [B]
- *   logp_pol, logp_ref  float32 [N]  written; 0 at masked rows
+ *   logp_pol, logp_ref  float32 [N]  written; 0 at masked rows (with
+ *                                    ref_logp_given, logp_ref is read, not
+ *                                    written)
  *   lse_pol             float32 [N]  written; the policy logsumexp, needed by
  *                                    grpo_loss_bwd; unspecified at masked rows
  *   loss                float32 [1]  written

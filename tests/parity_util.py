@@ -26,20 +26,25 @@ def oracle_adv(w: WL.Workload, inp) -> np.ndarray:
 
 def gpu_run(w: WL.Workload, inp, adv32: torch.Tensor, chunk_rows: int = 0, beta=None,
             grad: float = 1.0, H_ref=None, ids=None, mask=None, want_bwd: bool = True,
-            check: bool = True, want_dW: bool = False):
+            check: bool = True, want_dW: bool = False, logp_ref_given=None, **variant):
     """Forward (+ backward) through the library; returns host tensors."""
     import grpo_loss_gb300 as G
     dev = torch.device("cuda")
     eng = G.GRPOLoss(w.B, w.T, w.d, w.V, w.G, beta=w.beta if beta is None else beta,
                      eps=w.eps, std_unbiased=w.std_unbiased, chunk_rows=chunk_rows,
-                     dtype=torch_dtype(w), device=dev, compute_dW=want_dW)
+                     dtype=torch_dtype(w), device=dev, compute_dW=want_dW,
+                     ref_logp_given=logp_ref_given is not None, **variant)
     Hp = inp["H_pol"].to(dev)
     Hr = (inp["H_ref"] if H_ref is None else H_ref).to(dev)
     Wd = inp["W"].to(dev)
     idd = (inp["ids"] if ids is None else ids).to(dev)
     md = (inp["mask"] if mask is None else mask).to(dev)
     adv = adv32.to(dev)
-    loss, klm, lp, lr = eng.forward(Hp, Hr, Wd, idd, md, adv)
+    if logp_ref_given is not None:
+        loss, klm, lp, lr = eng.forward(Hp, None, Wd, idd, md, adv,
+                                        logp_ref=logp_ref_given.to(dev))
+    else:
+        loss, klm, lp, lr = eng.forward(Hp, Hr, Wd, idd, md, adv)
     out = {}
     if want_bwd:
         dH = eng.backward(Hp, Wd, idd, md, adv, grad)
