@@ -151,11 +151,12 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def _flops(w, n_valid, dW=False):
-    # 2 N d V per logit GEMM: policy + reference forward, policy recompute, dH
-    # (and dW when requested)
+def _flops(w, n_valid, dW=False, ref_given=False):
+    # 2 N d V per logit GEMM: policy (+ reference) forward, policy recompute,
+    # dH (and dW when requested)
     unit = 2.0 * n_valid * w.d * w.V
-    return {"step": (5.0 if dW else 4.0) * unit, "fwd_gemm_lse": 2.0 * unit,
+    sides = 1.0 if ref_given else 2.0
+    return {"step": (sides + 2.0 + (1.0 if dW else 0.0)) * unit, "fwd_gemm_lse": sides * unit,
             "bwd_dz_gemm": unit, "bwd_dh_gemm": unit, "bwd_dw_gemm": unit}
 
 
@@ -264,16 +265,27 @@ def run_ours(args, w):
     dt = torch.float32 if w.dtype == "f32" else torch.bfloat16
 
     eng = G.GRPOLoss(w.B, w.T, w.d, w.V, w.G, beta=w.beta, eps=w.eps,
-                     std_unbiased=w.std_unbiased, dtype=dt, device=dev, compute_dW=args.dW)
+                     std_unbiased=w.std_unbiased, dtype=dt, device=dev, compute_dW=args.dW,
+                     token_level=args.token_level, softcap=args.softcap,
+                     temperature=args.temperature, ref_logp_given=args.ref_given)
     d_in = {k: (v.to(dev) if v is not None else None) for k, v in inp.items()}
     rewards = d_in["rewards"]
     adv_in = d_in["adv"]
     dH = torch.empty_like(d_in["H_pol"])
     stream = torch.cuda.current_stream()
 
+    if args.ref_given:
+        # reference log-probs a trainer kept from generation time; any float32
+        # values serve for timing (the kernels' work does not depend on them)
+        d_in["logp_ref"] = torch.full((w.N,), -12.0, dtype=torch.float32, device=dev)
+
     def step(d):
         adv = adv_in if w.supplied_adv else eng.advantages(d["rewards"])
-        eng.forward(d["H_pol"], d["H_ref"], d["W"], d["ids"], d["mask"], adv)
+        if args.ref_given:
+            eng.forward(d["H_pol"], None, d["W"], d["ids"], d["mask"], adv,
+                        logp_ref=d["logp_ref"])
+        else:
+            eng.forward(d["H_pol"], d["H_ref"], d["W"], d["ids"], d["mask"], adv)
         eng.backward(d["H_pol"], d["W"], d["ids"], d["mask"], adv, 1.0, dH=dH)
 
     # ---------------------------------------------------------- device-resident
@@ -309,9 +321,10 @@ def run_ours(args, w):
     value = total_valid / (ms_step / 1e3)
 
     # --------------------------------------------------------------- end to end
-    host = {k: (v.pin_memory() if v is not None else None) for k, v in inp.items()}
+    e2e_src = dict(inp, H_ref=None, logp_ref=d_in["logp_ref"].cpu()) if args.ref_given else inp
+    host = {k: (v.pin_memory() if v is not None else None) for k, v in e2e_src.items()}
     d_e2e = {k: (torch.empty_like(v, device=dev) if v is not None else None)
-             for k, v in inp.items()}
+             for k, v in e2e_src.items()}
     loss_host = torch.empty(2, dtype=torch.float32).pin_memory()
     h2d = sum(v.numel() * v.element_size() for k, v in host.items() if v is not None)
     d2h = loss_host.numel() * loss_host.element_size()
@@ -341,7 +354,7 @@ def run_ours(args, w):
 
     if rank == 0:
         peaks = _peaks()
-        fl = _flops(w, n_valid, args.dW)
+        fl = _flops(w, n_valid, args.dW, args.ref_given)
         gemms = {k: prof[k] for k in ("fwd_gemm_lse", "bwd_dz_gemm", "bwd_dh_gemm",
                                       "bwd_dw_gemm") if prof[k][1]}
         dom = max(gemms, key=lambda k: gemms[k][0])
@@ -362,6 +375,9 @@ def run_ours(args, w):
             "config": {"workload": w.name, "prompts": w.prompts, "generations": w.G,
                        "completion_len": w.T, "tokens": w.N, "valid_tokens": n_valid,
                        "hidden": w.d, "vocab": w.V, "beta": w.beta, "dW": bool(args.dW),
+                       "variant": {"token_level": bool(args.token_level), "softcap": args.softcap,
+                                   "temperature": args.temperature,
+                                   "ref_logp_given": bool(args.ref_given)},
                        "flops_per_step": fl["step"],
                        "parallelism": "replicas" if ws > 1 else "single",
                        "l2": "inputs larger than L2 (H_pol+H_ref+W = %.2f GB)"
@@ -397,6 +413,11 @@ def main():
                     choices=sorted(list(WL.FULL) + list(WL.SMALL)))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--dW", action="store_true", help="also compute the lm_head gradient")
+    ap.add_argument("--token-level", action="store_true", help="token-level loss aggregation")
+    ap.add_argument("--softcap", type=float, default=0.0, help="logit softcap (0 = off)")
+    ap.add_argument("--temperature", type=float, default=0.0, help="logit temperature (0 = off)")
+    ap.add_argument("--ref-given", action="store_true",
+                    help="reference log-probs supplied; skip the reference GEMM half")
     args = ap.parse_args()
     w = WL.FULL.get(args.workload) or WL.SMALL[args.workload]
     if args.impl == "reference":
