@@ -76,6 +76,7 @@ _SIGNATURES = {
     "grpo_profile_collect": (ctypes.c_int, [ctypes.POINTER(ctypes.c_double),
                                             ctypes.POINTER(ctypes.c_int64), ctypes.c_int32]),
     "grpo_profile_kind_count": (ctypes.c_int32, []),
+    "grpo_test_pipeline_stall": (ctypes.c_int, [ctypes.c_int32, ctypes.c_uint32]),
     "grpo_profile_kind_name": (ctypes.c_char_p, [ctypes.c_int32]),
 }
 

@@ -13,6 +13,9 @@
 //             both operands are read as stored (MN-major), and the fp32
 //             result is accumulated into dW across chunks.
 //
+// mapA1 is the reference hidden states in MODE_FWD and the store map of the
+// dZ chunk (32 x 32 boxes, 64-byte swizzle) in MODE_DZ.
+//
 // One CTA per SM, 6 warps: warp 0 issues TMA loads into a 4-stage shared
 // memory ring, warp 1 owns tensor memory and issues the MMAs, warps 2..5 run
 // the epilogue, each thread owning one accumulator row (one TMEM lane).
@@ -33,8 +36,11 @@ constexpr int kThreads = 192;
 constexpr int kEpiThreads = 128;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kAccStride = 256;  // TMEM columns per accumulator buffer
-constexpr int kSmemBytes =
-    1024 + kStages * (kAStageBytes + kBStageBytes) + 256;  // alignment slack + ring + barriers
+// MODE_DZ output staging: per epilogue warp two 32-row x 64-byte tiles
+constexpr int kStageOutBytes = 32 * 64;
+constexpr int kOutBytes = 4 * 2 * kStageOutBytes;  // 16 KB
+constexpr int kSmemBytes = 1024 + kStages * (kAStageBytes + kBStageBytes) + kOutBytes +
+                           256;  // alignment slack + ring + output staging + barriers
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kMNBoxBytes = 64 * kBK * 2;  // one 64 (MN) x 64 (K) bf16 TMA box: 8 KB
 
@@ -102,8 +108,15 @@ __device__ __forceinline__ Unit unit_decode(const GemmArgs& g, int nb, int u) {
     r.row0 = g.blk[g.chunk_b0 + r.jj] * kBM;
     r.a_row = r.row0;
   } else if (MODE == MODE_DH) {
-    r.jj = u / g.n_nt;
-    r.t0 = u - r.jj * g.n_nt;
+    // column tiles in groups of g.nt_group: the resident units cover
+    // sms / nt_group blocks x nt_group column tiles, trading re-reads of the
+    // dZ rows (once per group) against re-reads of W^T (once per wave)
+    const int nbc = min(g.chunk_nb, nb - g.chunk_b0);
+    const int per_grp = nbc * g.nt_group;
+    const int grp = u / per_grp;
+    const int rem = u - grp * per_grp;
+    r.jj = rem / g.nt_group;
+    r.t0 = grp * g.nt_group + (rem - r.jj * g.nt_group);
     r.t1 = r.t0 + 1;
     r.side = 0;
     r.vs = 0;
@@ -149,7 +162,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* smA = smem;
   uint8_t* smB = smem + kStages * kAStageBytes;
-  Smem* sh = reinterpret_cast<Smem*>(smB + kStages * kBStageBytes);
+  uint8_t* smOut = smB + kStages * kBStageBytes;  // 1024-byte aligned
+  Smem* sh = reinterpret_cast<Smem*>(smOut + kOutBytes);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -202,9 +216,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int t = un.t0; ok && t < un.t1; ++t) {
           const int b_row = t * g.bn;
           for (int kb = 0; kb < nk; ++kb) {
-            if (!mbar_wait(&sh->empty[s], ph ^ 1u, abort)) {
+            if (!mbar_wait(&sh->empty[s], ph ^ 1u, abort, g.wait_ns)) {
               ok = false;
               break;
+            }
+            if (g.stall_test && blockIdx.x == 0 && u == static_cast<int>(blockIdx.x) &&
+                t == un.t0 && kb == 0) {
+              // Testing: this stage is never armed, so the MMA warp's wait on
+              // it expires and the CTA takes its abort path.
+              if (++s == kStages) {
+                s = 0;
+                ph ^= 1u;
+              }
+              continue;
             }
             mbar_arrive_expect_tx(&sh->full[s], kAStageBytes + b_bytes);
             if (kAMN) {
@@ -241,7 +265,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Drain: every load issued must have landed before the CTA exits.
       volatile int no_abort = 0;
       for (int st = 0; st < kStages; ++st)
-        if (issued & (1u << st)) mbar_wait(&sh->full[st], (last_par >> st) & 1u, &no_abort);
+        if (issued & (1u << st)) mbar_wait(&sh->full[st], (last_par >> st) & 1u, &no_abort, g.wait_ns);
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
@@ -255,14 +279,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int u = blockIdx.x; ok && u < n_units; u += gridDim.x) {
         const Unit un = unit_decode<MODE>(g, nb, u);
         for (int t = un.t0; ok && t < un.t1; ++t) {
-          if (!mbar_wait(&sh->acc_empty[ab], aph ^ 1u, abort)) {
+          if (!mbar_wait(&sh->acc_empty[ab], aph ^ 1u, abort, g.wait_ns)) {
             ok = false;
             break;
           }
           tc_fence_after();
           const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(ab * kAccStride);
           for (int kb = 0; kb < nk; ++kb) {
-            if (!mbar_wait(&sh->full[s], ph, abort)) {
+            if (!mbar_wait(&sh->full[s], ph, abort, g.wait_ns)) {
               ok = false;
               break;
             }
@@ -299,13 +323,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Every MMA issued must complete before tensor memory is released.
       umma_commit(&sh->mma_done);
       volatile int no_abort = 0;
-      mbar_wait(&sh->mma_done, 0, &no_abort);
+      mbar_wait(&sh->mma_done, 0, &no_abort, g.wait_ns);
     }
   } else {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;  // TMEM lane quadrant this warp may access
     const int r_in_tile = q * 32 + lane;
     const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+    // MODE_DZ: this warp's two staging tiles and the chunk counter picking one
+    uint8_t* my_out = smOut + (warp - 2) * 2 * kStageOutBytes;
+    uint32_t n_out = 0;
     int ab = 0;
     uint32_t aph = 0;
     bool ok = true;
@@ -334,7 +361,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       for (int t = un.t0; t < un.t1; ++t) {
         // warp-uniform outcome: the tensor-memory loads below are .sync.aligned
-        if (!__all_sync(0xffffffffu, mbar_wait(&sh->acc_full[ab], aph, abort))) {
+        if (!__all_sync(0xffffffffu, mbar_wait(&sh->acc_full[ab], aph, abort, g.wait_ns))) {
           ok = false;
           break;
         }
@@ -392,8 +419,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           s_comp = (tk - s_run) - yk;
           s_run = tk;
         } else if (MODE == MODE_DZ) {
-          __nv_bfloat16* dst =
-              g.dz + (static_cast<int64_t>(un.jj) * kBM + r_in_tile) * g.ldz;
+          // dZ rows of this warp in the chunk buffer: jj*128 + 32q .. +31
+          const int32_t out_y = un.jj * kBM + q * 32;
 #pragma unroll 1
           for (int c = 0; c < kVocabTile / 32; ++c) {
             const int64_t col0 = col_t + c * 32;
@@ -425,13 +452,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t pk[16];
 #pragma unroll
             for (int j = 0; j < 16; ++j) pk[j] = pack_bf16x2(o[2 * j], o[2 * j + 1]);
+            // Stage the warp's 32 x 32 bf16 block in shared memory with the
+            // 64-byte swizzle (16-byte piece v of row r lands at piece
+            // v ^ ((r >> 1) & 3)), then one lane stores it with TMA; columns
+            // at or past V are clipped by the tensor map.
+            uint8_t* buf = my_out + (n_out & 1u) * kStageOutBytes;
+            if (lane == 0) tma_store_wait_read_1();  // the store that used buf is done reading
+            __syncwarp();
 #pragma unroll
             for (int v = 0; v < 4; ++v) {
-              if (col0 + 8 * v < g.V) {
-                *reinterpret_cast<uint4*>(dst + col0 + 8 * v) =
-                    make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
-              }
+              const int pv = v ^ ((lane >> 1) & 3);
+              *reinterpret_cast<uint4*>(buf + lane * 64 + pv * 16) =
+                  make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
             }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&mapA1, buf, static_cast<int32_t>(col0), out_y);
+              tma_store_commit();
+            }
+            ++n_out;
           }
         } else if (MODE == MODE_DW) {
           const int ncc = g.bn / 32;
@@ -508,6 +548,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       set_error(g.err, ERRBIT_TIMEOUT);
       *abort = 1;
     }
+    // the staged dZ stores must have completed before the CTA exits
+    if (MODE == MODE_DZ && lane == 0) tma_store_wait_all();
   }
 
   tc_fence_before();

@@ -122,19 +122,26 @@ EncodeTiledFn encode_fn() {
 }
 
 // bf16 matrix [rows][inner] with row stride `ld` elements; box of
-// 64 x box_rows elements, 128-byte swizzle (the UMMA K-major layout).
-grpo_status make_map(CUtensorMap* m, const void* base, int64_t inner, int64_t rows, int64_t ld,
-                     int box_rows) {
+// box_inner x box_rows elements with the given swizzle.
+grpo_status make_map_box(CUtensorMap* m, const void* base, int64_t inner, int64_t rows,
+                         int64_t ld, int box_inner, int box_rows, CUtensorMapSwizzle swz) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return GRPO_ERR_CUDA;
   cuuint64_t gdim[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(rows)};
   cuuint64_t gstride[1] = {static_cast<cuuint64_t>(ld) * 2};
-  cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(box_inner), static_cast<cuuint32_t>(box_rows)};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), gdim, gstride,
-                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? GRPO_OK : GRPO_ERR_UNSUPPORTED;
+}
+
+// Operand map: box of 64 x box_rows elements, 128-byte swizzle (the UMMA
+// operand layout).
+grpo_status make_map(CUtensorMap* m, const void* base, int64_t inner, int64_t rows, int64_t ld,
+                     int box_rows) {
+  return make_map_box(m, base, inner, rows, ld, kBK, box_rows, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 // ------------------------------------------------------------------ plan
@@ -309,6 +316,15 @@ void set_xform(const grpo_problem* p, GemmArgs* g) {
   g->xform = (g->x_scale != 1.f || g->x_cap > 0.f || g->x_inv_temp != 1.f) ? 1 : 0;
 }
 
+// Testing hook state (grpo_test_pipeline_stall).
+struct TestHooks {
+  int stall = 0;
+  uint64_t wait_ns = 0;
+};
+TestHooks g_test;
+
+uint64_t wait_limit_ns() { return g_test.wait_ns ? g_test.wait_ns : 4000000000ull; }
+
 // Control block at the start of every workspace.
 struct Ctrl {
   uint32_t err;
@@ -431,6 +447,8 @@ grpo_status grpo_loss_fwd(const grpo_problem* problem, const void* H_pol, const 
   g.err = &ctrl->err;
   g.n_sides = ref_given ? 1 : 2;
   set_xform(problem, &g);
+  g.wait_ns = wait_limit_ns();
+  g.stall_test = g_test.stall;
   const int64_t units = static_cast<int64_t>(g.n_sides) * P.nblk_max * P.n_vs;
   const int grid = static_cast<int>(units < P.sms ? units : P.sms);
   LAUNCH(K_FWD_GEMM, stream, launch_gemm(MODE_FWD, mHp, mHr, mW, g, grid, stream));
@@ -490,8 +508,12 @@ grpo_status grpo_loss_bwd(const grpo_problem* problem, const void* H_pol, const 
   // K-major maps (box 64 x rows) for the recompute and dH; MN-major maps
   // (box 64 x 64) for dZ and H as dW's operands
   __nv_bfloat16* wt = reinterpret_cast<__nv_bfloat16*>(ws + P.b_wt);
-  CUtensorMap mHp, mW, mDz, mWt, mDzMn, mHmn;
+  CUtensorMap mHp, mW, mDz, mWt, mDzMn, mHmn, mDzStore;
   const int64_t dz_rows = static_cast<int64_t>(P.chunk_nb) * kBM;
+  // the dZ epilogue stores 32 x 32 boxes staged with the 64-byte swizzle
+  if ((st = make_map_box(&mDzStore, dz, P.V, dz_rows, P.ldv, 32, 32,
+                         CU_TENSOR_MAP_SWIZZLE_64B)) != GRPO_OK)
+    return st;
   if ((st = make_map(&mHp, hp, P.d, P.N, P.d, kBM)) != GRPO_OK) return st;
   if ((st = make_map(&mW, w, P.d, P.V, P.d, kVocabTile)) != GRPO_OK) return st;
   if ((st = make_map(&mDz, dz, P.V, dz_rows, P.ldv, kBM)) != GRPO_OK) return st;
@@ -523,6 +545,13 @@ grpo_status grpo_loss_bwd(const grpo_problem* problem, const void* H_pol, const 
   g.n_nt = P.n_nt;
   g.chunk_nb = P.chunk_nb;
   g.group_blocks = P.sms / 4 > 16 ? P.sms / 4 : 16;
+  // dH raster: at most 8 column tiles side by side (a divisor of n_nt)
+  g.nt_group = 1;
+  for (int q = 8; q >= 1; --q)
+    if (P.n_nt % q == 0) {
+      g.nt_group = q;
+      break;
+    }
   g.nblk_max = P.nblk_max;
   g.N = P.N;
   g.d = P.d;
@@ -538,6 +567,7 @@ grpo_status grpo_loss_bwd(const grpo_problem* problem, const void* H_pol, const 
   g.n_mt = P.n_mt;
   g.err = &ctrl->err;
   set_xform(problem, &g);
+  g.wait_ns = wait_limit_ns();
   const int64_t dz_units = static_cast<int64_t>(P.chunk_nb) * P.n_vt;
   const int64_t dh_units = static_cast<int64_t>(P.chunk_nb) * P.n_nt;
   const int grid_dz = static_cast<int>(dz_units < P.sms ? dz_units : P.sms);
@@ -549,7 +579,7 @@ grpo_status grpo_loss_bwd(const grpo_problem* problem, const void* H_pol, const 
     GemmArgs gz = g;
     gz.bn = kVocabTile;
     gz.nk = P.nk_d;
-    LAUNCH(K_BWD_DZ_GEMM, stream, launch_gemm(MODE_DZ, mHp, mHp, mW, gz, grid_dz, stream));
+    LAUNCH(K_BWD_DZ_GEMM, stream, launch_gemm(MODE_DZ, mHp, mDzStore, mW, gz, grid_dz, stream));
     GemmArgs gh = g;
     gh.bn = P.bn_dh;
     gh.nk = P.nk_v;
@@ -610,6 +640,12 @@ grpo_status grpo_profile_collect(double* ms, int64_t* launches, int32_t n_kinds)
   }
   g_prof.used = 0;
   return st;
+}
+
+grpo_status grpo_test_pipeline_stall(int32_t on, uint32_t wait_ms) {
+  g_test.stall = on ? 1 : 0;
+  g_test.wait_ns = static_cast<uint64_t>(wait_ms) * 1000000ull;
+  return GRPO_OK;
 }
 
 int32_t grpo_profile_kind_count(void) { return K_NUM_KINDS; }

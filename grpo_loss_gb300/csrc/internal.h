@@ -30,6 +30,7 @@ struct GemmArgs {
   int chunk_b0;           // MODE_DZ/DH: first compacted block of the chunk
   int chunk_nb;           // MODE_DZ/DH: blocks per chunk
   int group_blocks;       // MODE_DZ: blocks per raster group
+  int nt_group;           // MODE_DH: column tiles per raster group (divides n_nt)
   int nblk_max;           // ceil(N / 128)
   int64_t N, d, V;
   const int32_t* ids;
@@ -49,6 +50,8 @@ struct GemmArgs {
   float* dw;              // MODE_DW: dW [V][d], accumulated over chunks
   int n_mt;               // MODE_DW: 128-row vocab tiles
   uint32_t* err;          // device error word
+  uint64_t wait_ns;       // pipeline wait limit
+  int stall_test;         // testing: CTA 0 withholds its first stage (see grpo_test_pipeline_stall)
 };
 
 // Profiling kinds (one per kernel the library launches).

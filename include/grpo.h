@@ -221,6 +221,17 @@ grpo_status grpo_profile_collect(double *ms, int64_t *launches, int32_t n_kinds)
 int32_t grpo_profile_kind_count(void);
 const char *grpo_profile_kind_name(int32_t kind);
 
+/*
+ * Testing hook for the device-side failure path. With on = 1, the next
+ * forward GEMM launches withhold the first shared-memory stage of CTA 0, so
+ * that CTA's MMA wait expires: the kernel records GRPO_ERR_TIMEOUT in the
+ * workspace's error word, drains its copies, frees tensor memory and
+ * returns, and the context stays usable. wait_ms sets the pipeline wait
+ * limit of every kernel launched afterwards (0 restores the default of 4 s).
+ * Call with on = 0, wait_ms = 0 to restore normal operation. Not thread-safe.
+ */
+grpo_status grpo_test_pipeline_stall(int32_t on, uint32_t wait_ms);
+
 #ifdef __cplusplus
 }
 #endif

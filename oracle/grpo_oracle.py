@@ -49,6 +49,14 @@ Optional variants, all off by default:
 * Token-level aggregation: the loss is sum_n m_n l_n / sum_n m_n instead of
   the per-sequence mean averaged over sequences (the pages are silent on the
   aggregation; this is the other common GRPO normalisation).
+* KL variants from the pages' four experiments (zjt100.com page, "GRPO
+  的数学和发现的问题": the reference implementation; the detach removed; the
+  full reverse KL with the extra Q factor; forward KL instead). The page's
+  formulas are lost, so each is a reading: kl_mode 1 keeps the value of the
+  objective and drops the advantage term's gradient (exp(q - q) has none);
+  kl_mode 2 multiplies the estimator by Q(y) = exp(q); kl_mode 3 is the
+  forward-KL estimator under samples from Q, r log r - (r - 1) with
+  r = P/Q = exp(p - q).
 * Reference log-probabilities supplied by the caller instead of computed
   from H_ref (the reference model is frozen, so its log-probs can come from
   elsewhere, e.g. generation time).
@@ -174,16 +182,29 @@ def token_logprobs(H, W, ids, rows: Optional[Sequence[int]] = None, row_block: i
     return logp, lse
 
 
-def kl_estimator(logp_pol, logp_ref) -> np.ndarray:
-    """Reverse-KL estimator exp(x) - x - 1 with x = p - q, evaluated as
-    expm1(x) - x (the same number, without cancellation for small x)."""
-    x = np.asarray(logp_ref, np.float64) - np.asarray(logp_pol, np.float64)
-    return np.expm1(x) - x
+def kl_estimator(logp_pol, logp_ref, kl_mode: int = 0) -> np.ndarray:
+    """Per-token KL term with x = p - q.
+
+    kl_mode 0 and 1: the reverse-KL estimator exp(x) - x - 1, evaluated as
+    expm1(x) - x (the same number, without cancellation for small x);
+    kl_mode 2: exp(q) * (exp(x) - x - 1); kl_mode 3: x exp(x) - exp(x) + 1,
+    evaluated as x exp(x) - expm1(x).
+    """
+    q = np.asarray(logp_pol, np.float64)
+    x = np.asarray(logp_ref, np.float64) - q
+    k3 = np.expm1(x) - x
+    if kl_mode in (0, 1):
+        return k3
+    if kl_mode == 2:
+        return np.exp(q) * k3
+    if kl_mode == 3:
+        return x * np.exp(x) - np.expm1(x)
+    raise ValueError("kl_mode")
 
 
 def forward(H_pol, H_ref, W, ids, mask, adv, num_seqs: int, seq_len: int,
             beta: float, token_level: bool = False, xform=None,
-            logp_ref_given=None) -> Dict[str, np.ndarray]:
+            logp_ref_given=None, kl_mode: int = 0) -> Dict[str, np.ndarray]:
     """The GRPO loss forward pass over all N = num_seqs * seq_len tokens.
 
     Returns logp_pol, logp_ref, lse_pol (per token; log-probs are 0 at
@@ -203,7 +224,7 @@ def forward(H_pol, H_ref, W, ids, mask, adv, num_seqs: int, seq_len: int,
         p = to_f64(logp_ref_given).reshape(-1)
     q = np.where(m > 0, q, 0.0)
     p = np.where(m > 0, p, 0.0)
-    kl = np.where(m > 0, kl_estimator(q, p), 0.0)
+    kl = np.where(m > 0, kl_estimator(q, p, kl_mode), 0.0)
     w, cnt = sequence_weights(m, num_seqs, seq_len, token_level)
     A_tok = np.repeat(A, seq_len)
     # exp(q - q.detach()) has value 1, so the per-token loss is -(A - beta KL)
@@ -215,20 +236,32 @@ def forward(H_pol, H_ref, W, ids, mask, adv, num_seqs: int, seq_len: int,
             "cnt": cnt, "loss": loss, "kl_mean": kl_mean}
 
 
-def loss_coefficients(logp_pol, logp_ref, adv_tok, w, beta: float, grad_loss: float) -> np.ndarray:
-    """c_n = -dLoss/dq_n = g * w_n * (A_b + beta * (exp(x_n) - 1)), x = p - q.
+def loss_coefficients(logp_pol, logp_ref, adv_tok, w, beta: float, grad_loss: float,
+                      kl_mode: int = 0) -> np.ndarray:
+    """c_n = -dLoss/dq_n = g * w_n * (a_n - beta * dKL_n/dq_n), x = p - q.
 
-    Derivation: the per-token loss is -(A exp(q - sg(q)) - beta KL(x)); its
-    q-derivative is -A + beta dKL/dq with dKL/dq = 1 - exp(x).
+    The per-token loss is -(A exp(q - sg(q)) - beta KL), so a_n = A_b (0 for
+    kl_mode 1, where exp(q - q) carries no gradient) and
+    dKL/dq = 1 - exp(x) (modes 0, 1), -x exp(q) (mode 2), -x exp(x) (mode 3).
     """
-    x = np.asarray(logp_ref, np.float64) - np.asarray(logp_pol, np.float64)
-    return grad_loss * np.asarray(w, np.float64) * (np.asarray(adv_tok, np.float64) + beta * np.expm1(x))
+    q = np.asarray(logp_pol, np.float64)
+    x = np.asarray(logp_ref, np.float64) - q
+    a = np.zeros_like(x) if kl_mode == 1 else np.asarray(adv_tok, np.float64) * np.ones_like(x)
+    if kl_mode in (0, 1):
+        dk = -np.expm1(x)
+    elif kl_mode == 2:
+        dk = -x * np.exp(q)
+    elif kl_mode == 3:
+        dk = -x * np.exp(x)
+    else:
+        raise ValueError("kl_mode")
+    return grad_loss * np.asarray(w, np.float64) * (a - beta * dk)
 
 
 def backward(H_pol, H_ref, W, ids, mask, adv, num_seqs: int, seq_len: int, beta: float,
              grad_loss: float = 1.0, rows: Optional[Sequence[int]] = None,
              want_dW: bool = False, want_dZ: bool = False, row_block: int = 256,
-             token_level: bool = False, xform=None, logp_ref_given=None):
+             token_level: bool = False, xform=None, logp_ref_given=None, kl_mode: int = 0):
     """Gradients of the loss: dH_pol (rows requested, or all) and optionally dW.
 
     Per row: q and p from ``token_logprobs`` (the reference rows are needed
@@ -270,7 +303,7 @@ def backward(H_pol, H_ref, W, ids, mask, adv, num_seqs: int, seq_len: int, beta:
             p = np.zeros(0)
         p_full = np.zeros(rr.size)
         p_full[valid] = p
-        c = loss_coefficients(q, p_full, A[rr // seq_len], w[rr], beta, grad_loss)
+        c = loss_coefficients(q, p_full, A[rr // seq_len], w[rr], beta, grad_loss, kl_mode)
         c = np.where(valid, c, 0.0)
         dZ = np.exp(Z - lse[:, None])
         dZ[np.arange(rr.size), safe] -= 1.0

@@ -372,3 +372,57 @@ def test_given_reference_logprobs_equal_computed_ones():
     b2 = O.backward(P["Hp"], None, P["W"], P["ids"], P["mask"], P["A"], P["B"], P["T"], P["beta"],
                     logp_ref_given=f["logp_ref"])
     assert np.allclose(b1["dH"], b2["dH"], rtol=1e-14, atol=1e-18)
+
+
+# ------------------------------------------------------------ KL variants
+
+def _literal_kl_mode_loss(P, H, W, kl_mode):
+    B, T = P["B"], P["T"]
+    q = torch.log_softmax(H @ W.T, dim=1)[torch.arange(B * T), P["ids"]]
+    with torch.no_grad():
+        p = torch.log_softmax(P["Hr"] @ W.detach().T, dim=1)[torch.arange(B * T), P["ids"]]
+    A = torch.from_numpy(np.repeat(P["A"], T))
+    m = P["mask"].double()
+    if kl_mode == 1:
+        adv_term = torch.exp(q - q) * A                  # the detach removed
+    else:
+        adv_term = torch.exp(q - q.detach()) * A
+    k3 = torch.exp(p - q) - (p - q) - 1
+    if kl_mode in (0, 1):
+        kl = k3
+    elif kl_mode == 2:
+        kl = torch.exp(q) * k3                           # the extra Q factor
+    else:
+        r = torch.exp(p - q)                             # forward KL, samples from Q
+        kl = r * torch.log(r) - (r - 1)
+    obj = adv_term - P["beta"] * kl
+    per_seq = (obj * m).reshape(B, T).sum(1) / m.reshape(B, T).sum(1).clamp(min=1)
+    return -per_seq.mean()
+
+
+@pytest.mark.parametrize("kl_mode", [0, 1, 2, 3])
+def test_kl_modes_match_literal_autograd(kl_mode):
+    P = _problem()
+    H = P["Hp"].clone().requires_grad_(True)
+    W = P["W"].clone().requires_grad_(True)
+    L = _literal_kl_mode_loss(P, H, W, kl_mode)
+    L.backward()
+    f = O.forward(P["Hp"], P["Hr"], P["W"], P["ids"], P["mask"], P["A"], P["B"], P["T"],
+                  P["beta"], kl_mode=kl_mode)
+    assert abs(f["loss"] - L.item()) < 1e-13
+    b = O.backward(P["Hp"], P["Hr"], P["W"], P["ids"], P["mask"], P["A"], P["B"], P["T"],
+                   P["beta"], want_dW=True, kl_mode=kl_mode)
+    assert np.allclose(b["dH"], H.grad.numpy(), rtol=1e-10, atol=1e-16)
+    assert np.allclose(b["dW"], W.grad.numpy(), rtol=1e-10, atol=1e-16)
+
+
+def test_kl_mode_estimators_vanish_at_equal_policies_and_are_nonnegative():
+    x = np.linspace(-3, 3, 61)
+    q = -np.abs(x) - 2.0
+    for mode in (0, 2, 3):
+        k = O.kl_estimator(q, q + x, mode)
+        assert np.all(k >= -1e-15)
+        assert O.kl_estimator(q[:1], q[:1], mode)[0] == 0.0
+    # mode 3 small x: x^2/2 + x^3/3 + ...
+    s = np.array([1e-3, -2e-3])
+    assert np.allclose(O.kl_estimator(np.zeros(2), s, 3), s ** 2 / 2 + s ** 3 / 3, rtol=1e-5)
