@@ -183,6 +183,7 @@ grpo_status validate_problem(const grpo_problem* p) {
   if (p->compute_dW != 0 && p->compute_dW != 1) return GRPO_ERR_INVALID_ARG;
   if (p->token_level != 0 && p->token_level != 1) return GRPO_ERR_INVALID_ARG;
   if (p->ref_logp_given != 0 && p->ref_logp_given != 1) return GRPO_ERR_INVALID_ARG;
+  if (p->kl_mode < 0 || p->kl_mode > 3) return GRPO_ERR_INVALID_ARG;
   for (float v : {p->logit_multiply, p->logit_divide, p->softcap, p->temperature})
     if (!isfinite(v) || v < 0.f) return GRPO_ERR_INVALID_ARG;
   return GRPO_OK;
@@ -455,7 +456,8 @@ grpo_status grpo_loss_fwd(const grpo_problem* problem, const void* H_pol, const 
 
   LAUNCH(K_FWD_FINISH, stream,
          launch_fwd_finish(inv, mask, cnt, adv, zy, part, P.nblk_max, P.n_vs, P.N, P.B, P.T,
-                           problem->token_level, ref_given ? 1 : 0, logp_pol, logp_ref,
+                           problem->token_level, ref_given ? 1 : 0, problem->kl_mode,
+                           logp_pol, logp_ref,
                            lse_pol, partials, kFinishGrid, stream));
   LAUNCH(K_FWD_REDUCE, stream,
          launch_fwd_reduce(partials, kFinishGrid, cnt, P.B, problem->beta, problem->token_level,
@@ -530,7 +532,7 @@ grpo_status grpo_loss_bwd(const grpo_problem* problem, const void* H_pol, const 
          launch_block_plan(mask, P.N, P.nblk_max, blk, inv, &ctrl->nblk, stream));
   LAUNCH(K_BWD_COEF, stream,
          launch_bwd_coef(mask, cnt, adv, logp_pol, logp_ref, P.N, P.B, P.T, problem->beta,
-                         grad_loss, problem->token_level, coef, stream));
+                         grad_loss, problem->token_level, problem->kl_mode, coef, stream));
   LAUNCH(K_TRANSPOSE_W, stream, launch_transpose_w(W, P.f32, P.V, P.d, wt, P.ldv, stream));
   if (P.dw && cudaMemsetAsync(dW, 0, sizeof(float) * P.V * P.d, stream) != cudaSuccess)
     return GRPO_ERR_CUDA;

@@ -91,15 +91,15 @@ cudaError_t launch_block_plan(const uint8_t* mask, int64_t N, int nblk, int* blk
 cudaError_t launch_fwd_finish(const int* inv, const uint8_t* mask, const int* cnt,
                               const float* adv, const float* zy, const float2* part,
                               int nblk_max, int n_vs, int64_t N, int B, int T, int token_level,
-                              int ref_given, float* logp_pol, float* logp_ref, float* lse_pol,
-                              double* partials, int grid, cudaStream_t s);
+                              int ref_given, int kl_mode, float* logp_pol, float* logp_ref,
+                              float* lse_pol, double* partials, int grid, cudaStream_t s);
 cudaError_t launch_fwd_reduce(const double* partials, int nparts, const int* cnt, int B,
                               float beta, int token_level, float* loss, float* kl_mean,
                               cudaStream_t s);
 cudaError_t launch_bwd_coef(const uint8_t* mask, const int* cnt, const float* adv,
                             const float* logp_pol, const float* logp_ref, int64_t N, int B,
-                            int T, float beta, float grad, int token_level, float* coef,
-                            cudaStream_t s);
+                            int T, float beta, float grad, int token_level, int kl_mode,
+                            float* coef, cudaStream_t s);
 cudaError_t launch_transpose_w(const void* W, int w_f32, int64_t V, int64_t d,
                                __nv_bfloat16* Wt, int64_t ldwt, cudaStream_t s);
 cudaError_t launch_zero_invalid_rows(const int* inv, int64_t N, int64_t d, void* out,

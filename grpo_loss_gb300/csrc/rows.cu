@@ -158,6 +158,14 @@ __global__ void __launch_bounds__(1024) k_block_plan(const uint8_t* __restrict__
 // Merge the vocab-slice partials into each row's logsumexp, form q, p, the
 // KL estimator and the weighted loss terms. Per-CTA float64 partial sums
 // (sum w*A, sum w*KL, sum m*KL) go to `partials` for a fixed-order final sum.
+// Per-token KL term of the selected mode, x = p - q (see grpo_problem.kl_mode).
+__device__ __forceinline__ float kl_term(float q, float x, int kl_mode) {
+  const float k3 = __fsub_rn(expm1f(x), x);
+  if (kl_mode == 2) return __fmul_rn(expf(q), k3);
+  if (kl_mode == 3) return __fsub_rn(__fmul_rn(x, expf(x)), expm1f(x));
+  return k3;
+}
+
 // Rounding is spelled out (__fmaf_rn, __fadd_rn, __fmul_rn) so that every
 // inlined copy computes bit-identical results: equal policy and reference
 // rows then give exactly x = p - q = 0.
@@ -179,7 +187,7 @@ __global__ void k_fwd_finish(const int* __restrict__ inv, const uint8_t* __restr
                              const int* __restrict__ cnt, const float* __restrict__ adv,
                              const float* __restrict__ zy, const float2* __restrict__ part,
                              int nblk_max, int n_vs, int64_t N, int B, int T, int token_level,
-                             int ref_given, float* __restrict__ logp_pol,
+                             int ref_given, int kl_mode, float* __restrict__ logp_pol,
                              float* __restrict__ logp_ref, float* __restrict__ lse_pol,
                              double* __restrict__ partials) {
   __shared__ double red[3][32];
@@ -201,7 +209,7 @@ __global__ void k_fwd_finish(const int* __restrict__ inv, const uint8_t* __restr
         lp = q;
         lr = p;
         const float x = __fsub_rn(p, q);
-        const float kl = __fsub_rn(expm1f(x), x);
+        const float kl = kl_term(q, x, kl_mode);
         const int b = static_cast<int>(n / T);
         const double w =
             token_level ? 1.0 : 1.0 / (static_cast<double>(B) * max(cnt[b], 1));
@@ -269,7 +277,7 @@ __global__ void k_fwd_reduce(const double* __restrict__ partials, int nparts,
 __global__ void k_bwd_coef(const uint8_t* __restrict__ mask, const int* __restrict__ cnt,
                            const float* __restrict__ adv, const float* __restrict__ logp_pol,
                            const float* __restrict__ logp_ref, int64_t N, int B, int T,
-                           float beta, float grad, int token_level,
+                           float beta, float grad, int token_level, int kl_mode,
                            float* __restrict__ coef) {
   __shared__ int64_t s_tot[32];
   double w_tok = 0.0;
@@ -292,10 +300,19 @@ __global__ void k_bwd_coef(const uint8_t* __restrict__ mask, const int* __restri
       const int b = static_cast<int>(n / T);
       const double w =
           token_level ? w_tok : 1.0 / (static_cast<double>(B) * max(cnt[b], 1));
-      const float x = logp_ref[n] - logp_pol[n];
+      // c = g w (a - beta dKL/dq); a = A_b except without the detach
+      const float q = logp_pol[n];
+      const float x = logp_ref[n] - q;
+      float mdk;  // -dKL/dq
+      if (kl_mode == 2)
+        mdk = x * expf(q);
+      else if (kl_mode == 3)
+        mdk = x * expf(x);
+      else
+        mdk = expm1f(x);
+      const double a = kl_mode == 1 ? 0.0 : static_cast<double>(adv[b]);
       c = static_cast<float>(static_cast<double>(grad) * w *
-                             (static_cast<double>(adv[b]) +
-                              static_cast<double>(beta) * static_cast<double>(expm1f(x))));
+                             (a + static_cast<double>(beta) * static_cast<double>(mdk)));
     }
     coef[n] = c;
   }
@@ -374,10 +391,10 @@ cudaError_t launch_block_plan(const uint8_t* mask, int64_t N, int nblk, int* blk
 cudaError_t launch_fwd_finish(const int* inv, const uint8_t* mask, const int* cnt,
                               const float* adv, const float* zy, const float2* part,
                               int nblk_max, int n_vs, int64_t N, int B, int T, int token_level,
-                              int ref_given, float* logp_pol, float* logp_ref, float* lse_pol,
-                              double* partials, int grid, cudaStream_t s) {
+                              int ref_given, int kl_mode, float* logp_pol, float* logp_ref,
+                              float* lse_pol, double* partials, int grid, cudaStream_t s) {
   k_fwd_finish<<<grid, 256, 0, s>>>(inv, mask, cnt, adv, zy, part, nblk_max, n_vs, N, B, T,
-                                    token_level, ref_given, logp_pol, logp_ref, lse_pol,
+                                    token_level, ref_given, kl_mode, logp_pol, logp_ref, lse_pol,
                                     partials);
   return cudaGetLastError();
 }
@@ -391,11 +408,11 @@ cudaError_t launch_fwd_reduce(const double* partials, int nparts, const int* cnt
 
 cudaError_t launch_bwd_coef(const uint8_t* mask, const int* cnt, const float* adv,
                             const float* logp_pol, const float* logp_ref, int64_t N, int B,
-                            int T, float beta, float grad, int token_level, float* coef,
-                            cudaStream_t s) {
+                            int T, float beta, float grad, int token_level, int kl_mode,
+                            float* coef, cudaStream_t s) {
   const int blocks = static_cast<int>(std::min<int64_t>((N + 255) / 256, 4096));
   k_bwd_coef<<<blocks, 256, 0, s>>>(mask, cnt, adv, logp_pol, logp_ref, N, B, T, beta, grad,
-                                    token_level, coef);
+                                    token_level, kl_mode, coef);
   return cudaGetLastError();
 }
 

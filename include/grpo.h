@@ -89,6 +89,14 @@ typedef struct grpo_problem {
   int32_t ref_logp_given; /* 1: grpo_loss_fwd reads the reference log-probs
                              from logp_ref instead of computing them; H_ref
                              is not used and may be NULL */
+  int32_t kl_mode;      /* KL term, after the four experiments of the
+                           zjt100.com page ("GRPO 的数学和发现的问题"), whose
+                           formulas are lost (x = p - q):
+                           0: exp(x) - x - 1 (reference implementation);
+                           1: the same value, the advantage term without its
+                              detach (exp(q - q) * A: no gradient);
+                           2: exp(q) * (exp(x) - x - 1) (the extra Q factor);
+                           3: x exp(x) - exp(x) + 1 (forward KL under Q) */
 } grpo_problem;
 
 /*

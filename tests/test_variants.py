@@ -22,12 +22,13 @@ def _oxf(variant):
             "softcap": variant.get("softcap", 0.0), "temperature": variant.get("temperature", 0.0)}
 
 
-def _check(w, inp, adv32, res, token_level, xf, given=None, dW=False):
+def _check(w, inp, adv32, res, token_level, xf, given=None, dW=False, kl_mode=0):
     f = O.forward(inp["H_pol"], inp["H_ref"], inp["W"], inp["ids"], inp["mask"], adv32.double(),
-                  w.B, w.T, w.beta, token_level=token_level, xform=xf, logp_ref_given=given)
+                  w.B, w.T, w.beta, token_level=token_level, xform=xf, logp_ref_given=given,
+                  kl_mode=kl_mode)
     g = O.backward(inp["H_pol"], inp["H_ref"], inp["W"], inp["ids"], inp["mask"], adv32.double(),
                    w.B, w.T, w.beta, token_level=token_level, xform=xf, logp_ref_given=given,
-                   want_dW=dW)
+                   want_dW=dW, kl_mode=kl_mode)
     m = inp["mask"].numpy() > 0
     assert rel_err(res["logp_pol"].numpy()[m], f["logp_pol"][m]) < TOL_REL
     assert rel_err(res["logp_ref"].numpy()[m], f["logp_ref"][m]) < TOL_REL
@@ -47,6 +48,10 @@ CASES = [
     ("softcap-only-tiny", WL.TINY, {"softcap": 1.0}),
     ("temperature-only", WL.SMALL["qwen3-small"], {"temperature": 0.6}),
     ("all", WL.SMALL["gpt-oss-small"], dict(XF, token_level=True)),
+    ("kl-no-detach", WL.SMALL["qwen2.5-small"], {"kl_mode": 1}),
+    ("kl-times-q", WL.SMALL["qwen2.5-small"], {"kl_mode": 2}),
+    ("kl-forward", WL.SMALL["llama3.1-small"], {"kl_mode": 3}),
+    ("kl-forward-token-softcap", WL.TINY, {"kl_mode": 3, "token_level": True, "softcap": 1.0}),
 ]
 
 
@@ -55,7 +60,8 @@ def test_variant_matches_oracle(name, w, variant):
     inp = WL.make_inputs(w)
     adv32 = torch.from_numpy(oracle_adv(w, inp)).float()
     res = gpu_run(w, inp, adv32, chunk_rows=256, want_dW=True, **variant)
-    _check(w, inp, adv32, res, variant.get("token_level", False), _oxf(variant), dW=True)
+    _check(w, inp, adv32, res, variant.get("token_level", False), _oxf(variant), dW=True,
+           kl_mode=variant.get("kl_mode", 0))
 
 
 @pytest.mark.parametrize("variant", [{}, dict(XF, token_level=True)], ids=["plain", "all"])
