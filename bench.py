@@ -413,6 +413,12 @@ def run_ours(args, w):
                          "traffic": measured_traffic(dom, w.name),
                          "peak_kind": "bf16 sustained (%s)" % peaks["source"]},
             "kernels": kernels,
+            "memory": {
+                "fwd_workspace_bytes": eng.ws_fwd.numel(),
+                "bwd_workspace_bytes": eng.ws_bwd.numel(),
+                # what an unfused loss would hold: fp32 logits of policy and reference
+                "unfused_fp32_logits_bytes": 2 * w.N * w.V * 4,
+            },
             "gpu_launches": launches,
             "clocks": clk,
             "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,

@@ -3,6 +3,8 @@
 #include <math.h>
 #include <string.h>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include <mutex>
 #include <vector>
 
@@ -66,6 +68,13 @@ void prof_end(cudaStream_t s) {
     prof_end(stream);                      \
     if (e_ != cudaSuccess) return GRPO_ERR_CUDA; \
   } while (0)
+
+// NVTX range around one library call (visible in Nsight Systems timelines;
+// a no-op when no tool is attached).
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+};
 
 // ------------------------------------------------------- device properties
 struct DeviceInfo {
@@ -362,6 +371,7 @@ grpo_status grpo_workspace_size(const grpo_problem* problem, size_t* fwd_bytes,
 
 grpo_status grpo_advantages(const float* rewards, int32_t num_seqs, int32_t group_size,
                             float eps, int32_t std_unbiased, float* adv, cudaStream_t stream) {
+  NvtxRange nvtx_range("grpo_advantages");
   if (!rewards || !adv || num_seqs < 1 || group_size < 1 || num_seqs % group_size != 0)
     return GRPO_ERR_INVALID_ARG;
   const int unb = std_unbiased ? 1 : 0;
@@ -376,6 +386,7 @@ grpo_status grpo_loss_fwd(const grpo_problem* problem, const void* H_pol, const 
                           const float* adv, float* logp_pol, float* logp_ref, float* lse_pol,
                           float* loss, float* kl_mean, void* workspace, size_t workspace_bytes,
                           cudaStream_t stream) {
+  NvtxRange nvtx_range("grpo_loss_fwd");
   grpo_status st = validate_problem(problem);
   if (st != GRPO_OK) return st;
   const bool ref_given = problem->ref_logp_given != 0;
@@ -470,6 +481,7 @@ grpo_status grpo_loss_bwd(const grpo_problem* problem, const void* H_pol, const 
                           const float* logp_pol, const float* logp_ref, const float* lse_pol,
                           float grad_loss, void* dH, float* dW, void* workspace,
                           size_t workspace_bytes, cudaStream_t stream) {
+  NvtxRange nvtx_range("grpo_loss_bwd");
   grpo_status st = validate_problem(problem);
   if (st != GRPO_OK) return st;
   if (!H_pol || !W || !ids || !mask || !adv || !logp_pol || !logp_ref || !lse_pol || !dH)
@@ -577,6 +589,7 @@ grpo_status grpo_loss_bwd(const grpo_problem* problem, const void* H_pol, const 
   const int64_t dw_units = static_cast<int64_t>(P.n_mt) * P.n_nt;
   const int grid_dw = static_cast<int>(dw_units < P.sms ? dw_units : P.sms);
   for (int c = 0; c < P.n_chunks; ++c) {
+    NvtxRange nvtx_chunk("grpo_bwd_chunk");
     g.chunk_b0 = c * P.chunk_nb;
     GemmArgs gz = g;
     gz.bn = kVocabTile;
