@@ -244,6 +244,32 @@ def run_reference(args, w):
     print(json.dumps(line), flush=True)
 
 
+def _gpu_numa_cpus(device_index: int):
+    """(NUMA node, CPU ids) of the host node the GPU is attached to, from
+    its PCI device in sysfs; (None, None) when that cannot be read."""
+    try:
+        uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+        sel = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+        out = subprocess.run(["nvidia-smi", "--query-gpu=pci.bus_id", "--format=csv,noheader",
+                              "-i", sel], capture_output=True, text=True, timeout=20)
+        bus = out.stdout.strip().splitlines()[0].strip().lower()
+        dom, rest = bus.split(":", 1)
+        bus = "%04x:%s" % (int(dom, 16), rest)
+        with open("/sys/bus/pci/devices/%s/numa_node" % bus) as fh:
+            node = int(fh.read().strip())
+        if node < 0:
+            return None, None
+        with open("/sys/devices/system/node/node%d/cpulist" % node) as fh:
+            cpus = set()
+            for part in fh.read().strip().split(","):
+                a, _, b = part.partition("-")
+                cpus.update(range(int(a), int(b or a) + 1))
+        cpus &= os.sched_getaffinity(0)
+        return (node, cpus) if cpus else (None, None)
+    except Exception:
+        return None, None
+
+
 def replica_workload(w, rank: int):
     """Rank r's independent batch: the same recipe with its own seed."""
     return w if rank == 0 else WL.Workload(**{**w.__dict__, "seed": w.seed + 100 * rank})
@@ -325,7 +351,16 @@ def run_ours(args, w):
     # back, as a training loop would. Two device copies of the inputs let the
     # copies of step i + 1 run on a copy stream while step i computes.
     e2e_src = dict(inp, H_ref=None, logp_ref=d_in["logp_ref"].cpu()) if args.ref_given else inp
-    host = {k: (v.pin_memory() if v is not None else None) for k, v in e2e_src.items()}
+    # pin the host buffers on the NUMA node the GPU is attached to (the
+    # pages come from the allocating thread's node), then restore affinity
+    node, cpus = _gpu_numa_cpus(local)
+    saved_aff = os.sched_getaffinity(0)
+    if cpus:
+        os.sched_setaffinity(0, cpus)
+    try:
+        host = {k: (v.pin_memory() if v is not None else None) for k, v in e2e_src.items()}
+    finally:
+        os.sched_setaffinity(0, saved_aff)
     bufs = [{k: (torch.empty_like(v, device=dev) if v is not None else None)
              for k, v in e2e_src.items()} for _ in range(2)]
     n_res = max(args.steps, args.warmup, 1)
@@ -425,7 +460,8 @@ def run_ours(args, w):
                     "d2h_bytes_per_step": d2h,
                     "mode": "pinned host inputs copied every step on a copy stream, "
                             "overlapping the previous step's compute; loss read back "
-                            "every step"},
+                            "every step",
+                    "host_numa_node": node},
             "cpu_baseline": cpu,
         }
         print(json.dumps(line), flush=True)

@@ -83,3 +83,28 @@ def test_reference_equal_policy_full_size(case):
     expect = -adv32.double()[cnt].sum().item() / w.B
     assert res["kl_mean"] == 0.0
     assert abs(res["loss"] - expect) <= 1e-6 * max(1.0, abs(expect))
+
+
+@pytest.mark.parametrize("variant", [{"softcap": 30.0, "temperature": 0.7, "token_level": True},
+                                     {"kl_mode": 3}], ids=["softcap-temp-token", "forward-kl"])
+def test_variant_sampled_rows_full_size(variant):
+    """A variant at the full Llama-shaped size: sampled rows against the oracle."""
+    w = WL.LLAMA31_8B_20K
+    inp = WL.make_inputs(w)
+    adv32 = torch.from_numpy(oracle_adv(w, inp)).float()
+    res = gpu_run(w, inp, adv32, **variant)
+    xf = None
+    if "softcap" in variant:
+        xf = {"softcap": variant["softcap"], "temperature": variant["temperature"]}
+    rows = WL.sample_rows(w, inp["mask"], count=48)
+    Wf = O.to_f64(inp["W"])
+    q, lse = O.token_logprobs(inp["H_pol"], Wf, inp["ids"], rows=rows, xform=xf)
+    p, _ = O.token_logprobs(inp["H_ref"], Wf, inp["ids"], rows=rows, xform=xf)
+    assert rel_err(res["logp_pol"].numpy()[rows], q) < TOL_REL
+    assert rel_err(res["logp_ref"].numpy()[rows], p) < TOL_REL
+    g = O.backward(inp["H_pol"], inp["H_ref"], Wf, inp["ids"], inp["mask"], adv32.double(),
+                   w.B, w.T, w.beta, rows=rows, token_level=variant.get("token_level", False),
+                   xform=xf, kl_mode=variant.get("kl_mode", 0))
+    assert rel_l2(res["dH"].numpy()[rows], g["dH"]) < TOL_DH_L2
+    del res
+    torch.cuda.empty_cache()
