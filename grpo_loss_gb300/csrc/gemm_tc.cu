@@ -9,12 +9,14 @@
 //   MODE_DH   dH = dZ W for the same chunk (K = V), stored in H's dtype,
 //             with B = W^T [d, V] (K-major; transposed once per call, which
 //             measured faster than reading W MN-major).
-//   MODE_DW   dW += dZ^T H_pol for the same chunk (K = the chunk's tokens);
-//             both operands are read as stored (MN-major), and the fp32
+//   MODE_DW   dW += dZ^T H_pol for the same chunk (K = the chunk's tokens),
+//             from the transposed copies dZ^T (written by the MODE_DZ
+//             epilogue) and H_pol^T, so both operands are K-major; the fp32
 //             result is accumulated into dW across chunks.
 //
 // mapA1 is the reference hidden states in MODE_FWD and the store map of the
-// dZ chunk (32 x 32 boxes, 64-byte swizzle) in MODE_DZ.
+// dZ chunk (32 x 32 boxes, 64-byte swizzle) in MODE_DZ; mapC is the store map
+// of dZ^T in MODE_DZ when dW is requested.
 //
 // One CTA per SM, 6 warps: warp 0 issues TMA loads into a 4-stage shared
 // memory ring, warp 1 owns tensor memory and issues the MMAs, warps 2..5 run
@@ -36,20 +38,13 @@ constexpr int kThreads = 192;
 constexpr int kEpiThreads = 128;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kAccStride = 256;  // TMEM columns per accumulator buffer
-// MODE_DZ output staging: per epilogue warp two 32-row x 64-byte tiles
+// MODE_DZ output staging: per epilogue warp two 32 x 32 bf16 tiles for dZ
+// and two for dZ^T (double-buffered), 64 bytes per tile row
 constexpr int kStageOutBytes = 32 * 64;
-constexpr int kOutBytes = 4 * 2 * kStageOutBytes;  // 16 KB
+constexpr int kOutBytes = 4 * 4 * kStageOutBytes;  // 32 KB
 constexpr int kSmemBytes = 1024 + kStages * (kAStageBytes + kBStageBytes) + kOutBytes +
                            256;  // alignment slack + ring + output staging + barriers
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr int kMNBoxBytes = 64 * kBK * 2;  // one 64 (MN) x 64 (K) bf16 TMA box: 8 KB
-
-// Which operands a mode reads MN-major (contiguous along M or N).
-template <int MODE>
-struct Major {
-  static constexpr bool a_mn = MODE == MODE_DW;
-  static constexpr bool b_mn = MODE == MODE_DW;
-};
 
 struct Smem {
   uint64_t full[kStages];
@@ -156,7 +151,8 @@ __device__ __forceinline__ float xform_logit(const GemmArgs& g, float z, float* 
 template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
     k_gemm(const __grid_constant__ CUtensorMap mapA0, const __grid_constant__ CUtensorMap mapA1,
-           const __grid_constant__ CUtensorMap mapB, const GemmArgs g) {
+           const __grid_constant__ CUtensorMap mapB, const __grid_constant__ CUtensorMap mapC,
+           const GemmArgs g) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -194,10 +190,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int nb = *g.nblk_dev;
   const int n_units = unit_count<MODE>(g, nb);
   const uint32_t b_bytes = static_cast<uint32_t>(g.bn) * kBK * 2;
-  // MODE_DW reduces over the chunk's tokens: two 64-row K blocks per block
+  // MODE_DW reduces over the chunk's tokens: two 64-wide K blocks per block
   const int nk = MODE == MODE_DW ? 2 * max(0, min(g.chunk_nb, nb - g.chunk_b0)) : g.nk;
-  constexpr bool kAMN = Major<MODE>::a_mn;
-  constexpr bool kBMN = Major<MODE>::b_mn;
+  const int b_k0 = MODE == MODE_DW ? g.chunk_b0 * kBM : 0;  // B's K offset (H^T columns)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -231,24 +226,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               continue;
             }
             mbar_arrive_expect_tx(&sh->full[s], kAStageBytes + b_bytes);
-            if (kAMN) {
-              // dZ chunk rows kb*64.. as K, two 64-wide vocab columns as M
-#pragma unroll
-              for (int i = 0; i < kBM / 64; ++i)
-                tma_load_2d(smA + s * kAStageBytes + i * kMNBoxBytes, mA, &sh->full[s],
-                            un.a_row + 64 * i, kb * kBK);
-            } else {
-              tma_load_2d(smA + s * kAStageBytes, mA, &sh->full[s], kb * kBK, un.a_row);
-            }
-            if (kBMN) {
-              // K rows: the chunk's token rows of H (two 64-row halves per block)
-              const int k_row = g.blk[g.chunk_b0 + (kb >> 1)] * kBM + (kb & 1) * 64;
-              for (int i = 0; i < g.bn / 64; ++i)
-                tma_load_2d(smB + s * kBStageBytes + i * kMNBoxBytes, &mapB, &sh->full[s],
-                            b_row + 64 * i, k_row);
-            } else {
-              tma_load_2d(smB + s * kBStageBytes, &mapB, &sh->full[s], kb * kBK, b_row);
-            }
+            tma_load_2d(smA + s * kAStageBytes, mA, &sh->full[s], kb * kBK, un.a_row);
+            tma_load_2d(smB + s * kBStageBytes, &mapB, &sh->full[s], b_k0 + kb * kBK, b_row);
             issued |= 1u << s;
             last_par = (last_par & ~(1u << s)) | (ph << s);
             if (++s == kStages) {
@@ -270,7 +249,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      const uint32_t idesc = idesc_bf16_f32(kBM, static_cast<uint32_t>(g.bn), kAMN, kBMN);
+      const uint32_t idesc = idesc_bf16_f32(kBM, static_cast<uint32_t>(g.bn));
       int s = 0;
       uint32_t ph = 0;
       int ab = 0;
@@ -295,12 +274,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t b_addr = smem_u32(smB + s * kBStageBytes);
 #pragma unroll
             for (int k = 0; k < kBK / 16; ++k) {
-              // K step of 16: 32 bytes along a K-major row, 16 rows of 128 bytes MN-major
-              const uint64_t ad = kAMN ? sdesc_mnmajor_sw128(a_addr + k * 2048, kMNBoxBytes)
-                                       : sdesc_kmajor_sw128(a_addr + k * 32);
-              const uint64_t bd = kBMN ? sdesc_mnmajor_sw128(b_addr + k * 2048, kMNBoxBytes)
-                                       : sdesc_kmajor_sw128(b_addr + k * 32);
-              umma_bf16(d_tmem, ad, bd, idesc, (kb | k) != 0);
+              // K step of 16 elements: 32 bytes along the 128-byte swizzled rows
+              umma_bf16(d_tmem, sdesc_kmajor_sw128(a_addr + k * 32),
+                        sdesc_kmajor_sw128(b_addr + k * 32), idesc, (kb | k) != 0);
             }
             umma_commit(&sh->empty[s]);
             if (++s == kStages) {
@@ -330,8 +306,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = warp & 3;  // TMEM lane quadrant this warp may access
     const int r_in_tile = q * 32 + lane;
     const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
-    // MODE_DZ: this warp's two staging tiles and the chunk counter picking one
-    uint8_t* my_out = smOut + (warp - 2) * 2 * kStageOutBytes;
+    // MODE_DZ: this warp's staging tiles (dZ 0-1, dZ^T 2-3) and the chunk
+    // counter picking one of each pair
+    uint8_t* my_out = smOut + (warp - 2) * 4 * kStageOutBytes;
     uint32_t n_out = 0;
     int ab = 0;
     uint32_t aph = 0;
@@ -457,7 +434,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             // v ^ ((r >> 1) & 3)), then one lane stores it with TMA; columns
             // at or past V are clipped by the tensor map.
             uint8_t* buf = my_out + (n_out & 1u) * kStageOutBytes;
-            if (lane == 0) tma_store_wait_read_1();  // the store that used buf is done reading
+            uint8_t* tbuf = my_out + (2 + (n_out & 1u)) * kStageOutBytes;
+            // the bulk group of two chunks ago (which read buf and tbuf) is done
+            if (lane == 0) tma_store_wait_read_1();
             __syncwarp();
 #pragma unroll
             for (int v = 0; v < 4; ++v) {
@@ -465,10 +444,24 @@ __global__ void __launch_bounds__(kThreads, 1)
               *reinterpret_cast<uint4*>(buf + lane * 64 + pv * 16) =
                   make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
             }
+            if (g.dzt_on) {
+              // dZ^T tile: row j (vocab column) holds this warp's 32 tokens;
+              // this lane's token sits at byte 2 * lane of the row, in 16-byte
+              // piece (lane >> 3) ^ ((j >> 1) & 3) of the 64-byte swizzle
+#pragma unroll
+              for (int j = 0; j < 32; ++j) {
+                const uint32_t word = pk[j >> 1];
+                const unsigned short h =
+                    static_cast<unsigned short>((j & 1) ? (word >> 16) : (word & 0xFFFFu));
+                *reinterpret_cast<unsigned short*>(
+                    tbuf + j * 64 + (((lane >> 3) ^ ((j >> 1) & 3)) << 4) + (lane & 7) * 2) = h;
+              }
+            }
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
               tma_store_2d(&mapA1, buf, static_cast<int32_t>(col0), out_y);
+              if (g.dzt_on) tma_store_2d(&mapC, tbuf, out_y, static_cast<int32_t>(col0));
               tma_store_commit();
             }
             ++n_out;
@@ -581,16 +574,16 @@ cudaError_t gemm_configure() {
 }
 
 cudaError_t launch_gemm(int mode, const CUtensorMap& a0, const CUtensorMap& a1,
-                        const CUtensorMap& b, const GemmArgs& args, int grid,
-                        cudaStream_t stream) {
+                        const CUtensorMap& b, const CUtensorMap& c, const GemmArgs& args,
+                        int grid, cudaStream_t stream) {
   if (mode == MODE_FWD)
-    k_gemm<MODE_FWD><<<grid, kThreads, kSmemBytes, stream>>>(a0, a1, b, args);
+    k_gemm<MODE_FWD><<<grid, kThreads, kSmemBytes, stream>>>(a0, a1, b, c, args);
   else if (mode == MODE_DZ)
-    k_gemm<MODE_DZ><<<grid, kThreads, kSmemBytes, stream>>>(a0, a1, b, args);
+    k_gemm<MODE_DZ><<<grid, kThreads, kSmemBytes, stream>>>(a0, a1, b, c, args);
   else if (mode == MODE_DH)
-    k_gemm<MODE_DH><<<grid, kThreads, kSmemBytes, stream>>>(a0, a1, b, args);
+    k_gemm<MODE_DH><<<grid, kThreads, kSmemBytes, stream>>>(a0, a1, b, c, args);
   else
-    k_gemm<MODE_DW><<<grid, kThreads, kSmemBytes, stream>>>(a0, a1, b, args);
+    k_gemm<MODE_DW><<<grid, kThreads, kSmemBytes, stream>>>(a0, a1, b, c, args);
   return cudaGetLastError();
 }
 

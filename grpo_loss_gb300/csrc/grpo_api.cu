@@ -38,7 +38,7 @@ constexpr size_t kMaxProfiled = 65536;
 const char* kKindNames[K_NUM_KINDS] = {
     "advantages", "convert_bf16", "seq_count",  "block_plan",  "fwd_gemm_lse", "fwd_finish",
     "fwd_reduce", "bwd_coef",     "transpose_w", "zero_rows",  "bwd_dz_gemm",  "bwd_dh_gemm",
-    "bwd_dw_gemm"};
+    "bwd_dw_gemm", "transpose_h"};
 
 void prof_begin(int k, cudaStream_t s) {
   if (!g_prof.on || g_prof.used >= kMaxProfiled) return;
@@ -174,7 +174,7 @@ struct Plan {
   // forward workspace offsets
   size_t f_cnt, f_blk, f_inv, f_zy, f_part, f_partials, f_hp16, f_hr16, f_w16, f_total;
   // backward workspace offsets
-  size_t b_cnt, b_blk, b_inv, b_coef, b_wt, b_dz, b_hp16, b_w16, b_total;
+  size_t b_cnt, b_blk, b_inv, b_coef, b_wt, b_dz, b_dzt, b_ht, b_hp16, b_w16, b_total;
 };
 
 grpo_status validate_problem(const grpo_problem* p) {
@@ -305,6 +305,11 @@ grpo_status make_plan(const grpo_problem* p, Plan* pl) {
   P.b_coef = take(sizeof(float) * P.N);
   P.b_wt = take(2ull * P.d * P.ldv);
   P.b_dz = take(2ull * P.chunk_nb * kBM * P.ldv);
+  if (P.dw) {
+    // dW reads dZ^T [V][chunk rows] and the compacted H^T [d][nblk_max * 128]
+    P.b_dzt = take(2ull * P.V * P.chunk_nb * kBM);
+    P.b_ht = take(2ull * P.d * P.nblk_max * kBM);
+  }
   if (P.f32) {
     P.b_hp16 = take(2ull * P.N * P.d);
     P.b_w16 = take(2ull * P.V * P.d);
@@ -463,7 +468,7 @@ grpo_status grpo_loss_fwd(const grpo_problem* problem, const void* H_pol, const 
   g.stall_test = g_test.stall;
   const int64_t units = static_cast<int64_t>(g.n_sides) * P.nblk_max * P.n_vs;
   const int grid = static_cast<int>(units < P.sms ? units : P.sms);
-  LAUNCH(K_FWD_GEMM, stream, launch_gemm(MODE_FWD, mHp, mHr, mW, g, grid, stream));
+  LAUNCH(K_FWD_GEMM, stream, launch_gemm(MODE_FWD, mHp, mHr, mW, mW, g, grid, stream));
 
   LAUNCH(K_FWD_FINISH, stream,
          launch_fwd_finish(inv, mask, cnt, adv, zy, part, P.nblk_max, P.n_vs, P.N, P.B, P.T,
@@ -522,8 +527,11 @@ grpo_status grpo_loss_bwd(const grpo_problem* problem, const void* H_pol, const 
   // K-major maps (box 64 x rows) for the recompute and dH; MN-major maps
   // (box 64 x 64) for dZ and H as dW's operands
   __nv_bfloat16* wt = reinterpret_cast<__nv_bfloat16*>(ws + P.b_wt);
-  CUtensorMap mHp, mW, mDz, mWt, mDzMn, mHmn, mDzStore;
+  CUtensorMap mHp, mW, mDz, mWt, mDzStore, mDzT, mDzTStore, mHt;
   const int64_t dz_rows = static_cast<int64_t>(P.chunk_nb) * kBM;
+  __nv_bfloat16* dzt = P.dw ? reinterpret_cast<__nv_bfloat16*>(ws + P.b_dzt) : nullptr;
+  __nv_bfloat16* ht = P.dw ? reinterpret_cast<__nv_bfloat16*>(ws + P.b_ht) : nullptr;
+  const int64_t ht_cols = static_cast<int64_t>(P.nblk_max) * kBM;
   // the dZ epilogue stores 32 x 32 boxes staged with the 64-byte swizzle
   if ((st = make_map_box(&mDzStore, dz, P.V, dz_rows, P.ldv, 32, 32,
                          CU_TENSOR_MAP_SWIZZLE_64B)) != GRPO_OK)
@@ -532,9 +540,16 @@ grpo_status grpo_loss_bwd(const grpo_problem* problem, const void* H_pol, const 
   if ((st = make_map(&mW, w, P.d, P.V, P.d, kVocabTile)) != GRPO_OK) return st;
   if ((st = make_map(&mDz, dz, P.V, dz_rows, P.ldv, kBM)) != GRPO_OK) return st;
   if ((st = make_map(&mWt, wt, P.V, P.d, P.ldv, P.bn_dh)) != GRPO_OK) return st;
+  mDzTStore = mDzStore;  // placeholders when dW is off (not read)
+  mDzT = mDz;
+  mHt = mHp;
   if (P.dw) {
-    if ((st = make_map(&mDzMn, dz, P.V, dz_rows, P.ldv, 64)) != GRPO_OK) return st;
-    if ((st = make_map(&mHmn, hp, P.d, P.N, P.d, 64)) != GRPO_OK) return st;
+    // dZ^T [V][dz_rows]: stored by the dZ epilogue, read K-major by dW; H^T likewise
+    if ((st = make_map_box(&mDzTStore, dzt, dz_rows, P.V, dz_rows, 32, 32,
+                           CU_TENSOR_MAP_SWIZZLE_64B)) != GRPO_OK)
+      return st;
+    if ((st = make_map(&mDzT, dzt, dz_rows, P.V, dz_rows, kBM)) != GRPO_OK) return st;
+    if ((st = make_map(&mHt, ht, ht_cols, P.d, ht_cols, P.bn_dh)) != GRPO_OK) return st;
   }
 
   if (cudaMemsetAsync(ctrl, 0, sizeof(Ctrl), stream) != cudaSuccess) return GRPO_ERR_CUDA;
@@ -546,6 +561,10 @@ grpo_status grpo_loss_bwd(const grpo_problem* problem, const void* H_pol, const 
          launch_bwd_coef(mask, cnt, adv, logp_pol, logp_ref, P.N, P.B, P.T, problem->beta,
                          grad_loss, problem->token_level, problem->kl_mode, coef, stream));
   LAUNCH(K_TRANSPOSE_W, stream, launch_transpose_w(W, P.f32, P.V, P.d, wt, P.ldv, stream));
+  if (P.dw)
+    LAUNCH(K_TRANSPOSE_H, stream,
+           launch_transpose_h_compact(static_cast<const __nv_bfloat16*>(hp), P.N, P.d, blk,
+                                      &ctrl->nblk, P.nblk_max, ht, ht_cols, stream));
   if (P.dw && cudaMemsetAsync(dW, 0, sizeof(float) * P.V * P.d, stream) != cudaSuccess)
     return GRPO_ERR_CUDA;
   LAUNCH(K_ZERO_ROWS, stream, launch_zero_invalid_rows(inv, P.N, P.d, dH, P.f32, stream));
@@ -578,6 +597,7 @@ grpo_status grpo_loss_bwd(const grpo_problem* problem, const void* H_pol, const 
   g.out = dH;
   g.out_f32 = P.f32 ? 1 : 0;
   g.dw = dW;
+  g.dzt_on = P.dw ? 1 : 0;
   g.n_mt = P.n_mt;
   g.err = &ctrl->err;
   set_xform(problem, &g);
@@ -594,15 +614,15 @@ grpo_status grpo_loss_bwd(const grpo_problem* problem, const void* H_pol, const 
     GemmArgs gz = g;
     gz.bn = kVocabTile;
     gz.nk = P.nk_d;
-    LAUNCH(K_BWD_DZ_GEMM, stream, launch_gemm(MODE_DZ, mHp, mDzStore, mW, gz, grid_dz, stream));
+    LAUNCH(K_BWD_DZ_GEMM, stream, launch_gemm(MODE_DZ, mHp, mDzStore, mW, mDzTStore, gz, grid_dz, stream));
     GemmArgs gh = g;
     gh.bn = P.bn_dh;
     gh.nk = P.nk_v;
-    LAUNCH(K_BWD_DH_GEMM, stream, launch_gemm(MODE_DH, mDz, mDz, mWt, gh, grid_dh, stream));
+    LAUNCH(K_BWD_DH_GEMM, stream, launch_gemm(MODE_DH, mDz, mDz, mWt, mDz, gh, grid_dh, stream));
     if (P.dw) {
       GemmArgs gw = g;
       gw.bn = P.bn_dh;
-      LAUNCH(K_BWD_DW_GEMM, stream, launch_gemm(MODE_DW, mDzMn, mDzMn, mHmn, gw, grid_dw, stream));
+      LAUNCH(K_BWD_DW_GEMM, stream, launch_gemm(MODE_DW, mDzT, mDzT, mHt, mDzT, gw, grid_dw, stream));
     }
   }
   return GRPO_OK;

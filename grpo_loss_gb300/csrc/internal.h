@@ -47,6 +47,7 @@ struct GemmArgs {
   float x_scale;          // logit_multiply / logit_divide
   float x_cap;            // softcap (0 = off)
   float x_inv_temp;       // 1 / temperature
+  int dzt_on;             // MODE_DZ: also store dZ^T (for MODE_DW)
   float* dw;              // MODE_DW: dW [V][d], accumulated over chunks
   int n_mt;               // MODE_DW: 128-row vocab tiles
   uint32_t* err;          // device error word
@@ -69,6 +70,7 @@ enum KernelKind : int {
   K_BWD_DZ_GEMM,
   K_BWD_DH_GEMM,
   K_BWD_DW_GEMM,
+  K_TRANSPOSE_H,
   K_NUM_KINDS
 };
 
@@ -76,8 +78,8 @@ enum KernelKind : int {
 size_t gemm_smem_bytes();
 cudaError_t gemm_configure();  // sets the dynamic shared memory limit once
 cudaError_t launch_gemm(int mode, const CUtensorMap& a0, const CUtensorMap& a1,
-                        const CUtensorMap& b, const GemmArgs& args, int grid,
-                        cudaStream_t stream);
+                        const CUtensorMap& b, const CUtensorMap& c, const GemmArgs& args,
+                        int grid, cudaStream_t stream);
 
 // ---------------------------------------------------------------- rows.cu
 cudaError_t launch_advantages(const float* rewards, int B, int G, float eps, int unbiased,
@@ -102,6 +104,9 @@ cudaError_t launch_bwd_coef(const uint8_t* mask, const int* cnt, const float* ad
                             float* coef, cudaStream_t s);
 cudaError_t launch_transpose_w(const void* W, int w_f32, int64_t V, int64_t d,
                                __nv_bfloat16* Wt, int64_t ldwt, cudaStream_t s);
+cudaError_t launch_transpose_h_compact(const __nv_bfloat16* H, int64_t N, int64_t d,
+                                       const int* blk, const int* nblk_dev, int nblk_max,
+                                       __nv_bfloat16* Ht, int64_t ldht, cudaStream_t s);
 cudaError_t launch_zero_invalid_rows(const int* inv, int64_t N, int64_t d, void* out,
                                      int out_f32, cudaStream_t s);
 

@@ -159,22 +159,6 @@ __device__ __forceinline__ uint64_t sdesc_kmajor_sw128(uint32_t saddr) {
   return desc;
 }
 
-// Shared-memory matrix descriptor: MN-major operand tile made of 64-element
-// (128-byte) wide columns of the MN dimension, each written by one TMA box of
-// 64 x K rows with 128-byte swizzling. Consecutive K rows are 128 bytes
-// apart, 8-row groups 1024 bytes (stride byte offset), and neighbouring
-// 64-element MN columns `mn_stride` bytes (leading byte offset). Moving along
-// K by 16 rows is done by adding 16 * 128 bytes to the start.
-__device__ __forceinline__ uint64_t sdesc_mnmajor_sw128(uint32_t saddr, uint32_t mn_stride) {
-  uint64_t desc = 0;
-  desc |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);         // start address
-  desc |= static_cast<uint64_t>((mn_stride >> 4) & 0x3FFFu) << 16;  // leading byte offset
-  desc |= static_cast<uint64_t>(1024 >> 4) << 32;                  // stride byte offset
-  desc |= static_cast<uint64_t>(1) << 46;                          // descriptor version
-  desc |= static_cast<uint64_t>(2) << 61;                          // 128-byte swizzle
-  return desc;
-}
-
 // Instruction descriptor of kind::f16: bf16 A and B, f32 D, M x N tile; A and
 // B are K-major unless a_mn / b_mn select the MN-major (transposed) form.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t M, uint32_t N, bool a_mn = false,

@@ -344,6 +344,34 @@ __global__ void k_transpose_w(const Tin* __restrict__ W, int64_t V, int64_t d,
   }
 }
 
+// ----------------------------------------------------- compacted H^T
+// Ht[c][r] = H[src(r)][c] for compacted rows r in [0, nblk_max * 128): the
+// row of block blk[r / 128] at offset r % 128, or 0 past the valid blocks or
+// past N (those rows of dZ are 0, and 0 * garbage could be NaN).
+__global__ void k_transpose_h_compact(const __nv_bfloat16* __restrict__ H, int64_t N, int64_t d,
+                                      const int* __restrict__ blk, const int* nblk_dev,
+                                      __nv_bfloat16* __restrict__ Ht, int64_t ldht) {
+  __shared__ float tile[32][33];
+  const int nb = *nblk_dev;
+  const int64_t r0 = static_cast<int64_t>(blockIdx.x) * 32;  // compacted rows
+  const int64_t c0 = static_cast<int64_t>(blockIdx.y) * 32;  // hidden columns
+  for (int i = threadIdx.y; i < 32; i += blockDim.y) {
+    const int64_t r = r0 + i, c = c0 + threadIdx.x;
+    const int64_t jb = r / kBM;
+    float v = 0.f;
+    if (jb < nb && c < d) {
+      const int64_t src = static_cast<int64_t>(blk[jb]) * kBM + (r - jb * kBM);
+      if (src < N) v = __bfloat162float(H[src * d + c]);
+    }
+    tile[i][threadIdx.x] = v;
+  }
+  __syncthreads();
+  for (int i = threadIdx.y; i < 32; i += blockDim.y) {
+    const int64_t c = c0 + i, r = r0 + threadIdx.x;
+    if (c < d) Ht[c * ldht + r] = __float2bfloat16_rn(tile[threadIdx.x][i]);
+  }
+}
+
 // ------------------------------------------------------------ zero rows
 // Zero the output rows of every 128-row block that holds no valid token.
 __global__ void k_zero_invalid_rows(const int* __restrict__ inv, int64_t N, int64_t row_bytes,
@@ -425,6 +453,15 @@ cudaError_t launch_transpose_w(const void* W, int w_f32, int64_t V, int64_t d,
   else
     k_transpose_w<__nv_bfloat16>
         <<<grid, block, 0, s>>>(static_cast<const __nv_bfloat16*>(W), V, d, Wt, ldwt);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_transpose_h_compact(const __nv_bfloat16* H, int64_t N, int64_t d,
+                                       const int* blk, const int* nblk_dev, int nblk_max,
+                                       __nv_bfloat16* Ht, int64_t ldht, cudaStream_t s) {
+  dim3 grid(static_cast<unsigned>(nblk_max * (kBM / 32)), static_cast<unsigned>((d + 31) / 32));
+  dim3 block(32, 8);
+  k_transpose_h_compact<<<grid, block, 0, s>>>(H, N, d, blk, nblk_dev, Ht, ldht);
   return cudaGetLastError();
 }
 
