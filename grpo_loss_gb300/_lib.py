@@ -39,7 +39,8 @@ class Problem(ctypes.Structure):
                 ("dtype", ctypes.c_int32), ("token_level", ctypes.c_int32),
                 ("logit_multiply", ctypes.c_float), ("logit_divide", ctypes.c_float),
                 ("softcap", ctypes.c_float), ("temperature", ctypes.c_float),
-                ("ref_logp_given", ctypes.c_int32), ("kl_mode", ctypes.c_int32)]
+                ("ref_logp_given", ctypes.c_int32), ("kl_mode", ctypes.c_int32),
+                ("cta_pairs", ctypes.c_int32)]
 
 
 def make_problem(num_seqs: int, seq_len: int, d: int, V: int, group_size: int,
@@ -47,14 +48,16 @@ def make_problem(num_seqs: int, seq_len: int, d: int, V: int, group_size: int,
                  chunk_rows: int = 0, dtype=torch.bfloat16, compute_dW: int = 0,
                  token_level: bool = False, logit_multiply: float = 0.0,
                  logit_divide: float = 0.0, softcap: float = 0.0, temperature: float = 0.0,
-                 ref_logp_given: bool = False, kl_mode: int = 0) -> Problem:
+                 ref_logp_given: bool = False, kl_mode: int = 0,
+                 cta_pairs: bool = False) -> Problem:
     return Problem(N=num_seqs * seq_len, d=d, V=V, num_seqs=num_seqs, seq_len=seq_len,
                    group_size=group_size, beta=beta, eps=eps, std_unbiased=std_unbiased,
                    chunk_rows=chunk_rows, compute_dW=1 if compute_dW else 0,
                    dtype=GRPO_F32 if dtype == torch.float32 else GRPO_BF16,
                    token_level=1 if token_level else 0, logit_multiply=logit_multiply,
                    logit_divide=logit_divide, softcap=softcap, temperature=temperature,
-                   ref_logp_given=1 if ref_logp_given else 0, kl_mode=kl_mode)
+                   ref_logp_given=1 if ref_logp_given else 0, kl_mode=kl_mode,
+                   cta_pairs=1 if cta_pairs else 0)
 
 
 _lib = None

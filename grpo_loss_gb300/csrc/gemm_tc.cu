@@ -18,11 +18,20 @@
 // dZ chunk (32 x 32 boxes, 64-byte swizzle) in MODE_DZ; mapC is the store map
 // of dZ^T in MODE_DZ when dW is requested.
 //
-// One CTA per SM, 6 warps: warp 0 issues TMA loads into a 4-stage shared
-// memory ring, warp 1 owns tensor memory and issues the MMAs, warps 2..5 run
-// the epilogue, each thread owning one accumulator row (one TMEM lane).
-// Two 256-column accumulators in tensor memory let the epilogue of one tile
+// One CTA per SM, 6 warps: warp 0 issues TMA loads into a shared-memory
+// ring, warp 1 owns tensor memory and issues the MMAs, warps 2..5 run the
+// epilogue, each thread owning one accumulator row (one TMEM lane). Two
+// 256-column accumulators in tensor memory let the epilogue of one tile
 // overlap the MMAs of the next.
+//
+// PAIR = true runs CTA pairs (clusters of 2) on tcgen05 cta_group::2: a pair
+// computes a 256-row tile, each CTA holding its own 128 rows of A and half of
+// the B tile (6 stages of 32 KB instead of 4 of 48 KB). The even CTA arms the
+// full barrier for both CTAs' bytes (the odd CTA's TMA completes on it),
+// issues the MMAs and multicasts its commits to both CTAs; both CTAs'
+// epilogue threads arrive on the even CTA's accumulator-empty barrier. The
+// pair takes blocks 2p and 2p + 1; a missing partner block loads rows past
+// the end of its tensor (zeros) and writes nothing.
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -30,10 +39,8 @@ namespace grpo {
 
 namespace {
 
-constexpr int kStages = 4;
-constexpr int kBNMax = 256;
-constexpr int kAStageBytes = kBM * kBK * 2;     // 16 KB
-constexpr int kBStageBytes = kBNMax * kBK * 2;  // 32 KB
+constexpr int kMaxStages = 6;
+constexpr int kAStageBytes = kBM * kBK * 2;  // 16 KB
 constexpr int kThreads = 192;
 constexpr int kEpiThreads = 128;
 constexpr uint32_t kTmemCols = 512;
@@ -42,13 +49,21 @@ constexpr int kAccStride = 256;  // TMEM columns per accumulator buffer
 // and two for dZ^T (double-buffered), 64 bytes per tile row
 constexpr int kStageOutBytes = 32 * 64;
 constexpr int kOutBytes = 4 * 4 * kStageOutBytes;  // 32 KB
-constexpr int kSmemBytes = 1024 + kStages * (kAStageBytes + kBStageBytes) + kOutBytes +
-                           256;  // alignment slack + ring + output staging + barriers
 constexpr float kLog2e = 1.4426950408889634f;
 
+template <bool PAIR>
+struct Cfg {
+  static constexpr int kStages = PAIR ? 6 : 4;
+  static constexpr int kBRows = PAIR ? 128 : 256;  // B rows of one CTA per stage (max)
+  static constexpr int kBStageBytes = kBRows * kBK * 2;
+  // alignment slack + ring + output staging + barriers
+  static constexpr int kSmemBytes =
+      1024 + kStages * (kAStageBytes + kBStageBytes) + kOutBytes + 256;
+};
+
 struct Smem {
-  uint64_t full[kStages];
-  uint64_t empty[kStages];
+  uint64_t full[kMaxStages];
+  uint64_t empty[kMaxStages];
   uint64_t acc_full[2];
   uint64_t acc_empty[2];
   uint64_t mma_done;
@@ -64,67 +79,89 @@ struct Unit {
   int t0, t1;    // tile range [t0, t1) along N
   int vs;        // MODE_FWD: vocab slice
   int row0;      // first original row of the block (output rows)
+  bool valid;    // this CTA's block exists (false for a missing pair partner)
 };
 
-template <int MODE>
-__device__ __forceinline__ int unit_count(const GemmArgs& g, int nb) {
-  if (MODE == MODE_FWD) return g.n_sides * nb * g.n_vs;
-  const int nbc = min(g.chunk_nb, nb - g.chunk_b0);
-  if (nbc <= 0) return 0;
-  if (MODE == MODE_DW) return g.n_mt * g.n_nt;
-  return MODE == MODE_DZ ? nbc * g.n_vt : nbc * g.n_nt;
+// Block counts seen by a unit: blocks, or block pairs for PAIR.
+template <bool PAIR>
+__device__ __forceinline__ int per_unit(int n) {
+  return PAIR ? (n + 1) >> 1 : n;
 }
 
-template <int MODE>
-__device__ __forceinline__ Unit unit_decode(const GemmArgs& g, int nb, int u) {
+template <int MODE, bool PAIR>
+__device__ __forceinline__ int unit_count(const GemmArgs& g, int nb) {
+  if (MODE == MODE_FWD) return g.n_sides * per_unit<PAIR>(nb) * g.n_vs;
+  const int nbc = min(g.chunk_nb, nb - g.chunk_b0);
+  if (nbc <= 0) return 0;
+  if (MODE == MODE_DW) return per_unit<PAIR>(g.n_mt) * g.n_nt;
+  return MODE == MODE_DZ ? per_unit<PAIR>(nbc) * g.n_vt : per_unit<PAIR>(nbc) * g.n_nt;
+}
+
+// `rank` is the CTA's place in its pair (0 without PAIR): it takes block
+// 2 p + rank of the unit's block pair p.
+template <int MODE, bool PAIR>
+__device__ __forceinline__ Unit unit_decode(const GemmArgs& g, int nb, int u, int rank) {
   Unit r;
+  const int N32 = static_cast<int>(g.N);  // a row past every tensor of rows: loads zeros
   if (MODE == MODE_FWD) {
+    const int nbp = per_unit<PAIR>(nb);
     const int i = u / g.n_vs;
     r.vs = u - i * g.n_vs;
-    r.side = i >= nb ? 1 : 0;
-    r.jj = i - r.side * nb;
-    r.row0 = g.blk[r.jj] * kBM;
+    r.side = i >= nbp ? 1 : 0;
+    const int p = i - r.side * nbp;
+    r.jj = PAIR ? 2 * p + rank : p;
+    r.valid = r.jj < nb;
+    r.row0 = r.valid ? g.blk[r.jj] * kBM : N32;
     r.a_row = r.row0;
     r.t0 = static_cast<int>((static_cast<int64_t>(r.vs) * g.n_vt) / g.n_vs);
     r.t1 = static_cast<int>((static_cast<int64_t>(r.vs + 1) * g.n_vt) / g.n_vs);
   } else if (MODE == MODE_DZ) {
     const int nbc = min(g.chunk_nb, nb - g.chunk_b0);
-    // groups of g.group_blocks blocks walk the vocab tiles together, so each
-    // W tile is fetched once per group while the group's A blocks stay in L2
-    const int gsz_full = g.group_blocks * g.n_vt;
+    const int nbcp = per_unit<PAIR>(nbc);
+    const int grp_sz = per_unit<PAIR>(g.group_blocks);
+    // groups of blocks walk the vocab tiles together, so each W tile is
+    // fetched once per group while the group's A blocks stay in L2
+    const int gsz_full = grp_sz * g.n_vt;
     const int grp = u / gsz_full;
-    const int gb = min(g.group_blocks, nbc - grp * g.group_blocks);
+    const int gb = min(grp_sz, nbcp - grp * grp_sz);
     const int rem = u - grp * gsz_full;
-    r.jj = grp * g.group_blocks + rem % gb;
+    const int p = grp * grp_sz + rem % gb;
+    r.jj = PAIR ? 2 * p + rank : p;
+    r.valid = r.jj < nbc;
     r.t0 = rem / gb;
     r.t1 = r.t0 + 1;
     r.side = 0;
     r.vs = 0;
-    r.row0 = g.blk[g.chunk_b0 + r.jj] * kBM;
+    r.row0 = r.valid ? g.blk[g.chunk_b0 + r.jj] * kBM : N32;
     r.a_row = r.row0;
   } else if (MODE == MODE_DH) {
     // column tiles in groups of g.nt_group: the resident units cover
     // sms / nt_group blocks x nt_group column tiles, trading re-reads of the
     // dZ rows (once per group) against re-reads of W^T (once per wave)
     const int nbc = min(g.chunk_nb, nb - g.chunk_b0);
-    const int per_grp = nbc * g.nt_group;
+    const int per_grp = per_unit<PAIR>(nbc) * g.nt_group;
     const int grp = u / per_grp;
     const int rem = u - grp * per_grp;
-    r.jj = rem / g.nt_group;
-    r.t0 = grp * g.nt_group + (rem - r.jj * g.nt_group);
+    const int p = rem / g.nt_group;
+    r.jj = PAIR ? 2 * p + rank : p;
+    r.valid = r.jj < nbc;
+    r.t0 = grp * g.nt_group + (rem - p * g.nt_group);
     r.t1 = r.t0 + 1;
     r.side = 0;
     r.vs = 0;
-    r.row0 = g.blk[g.chunk_b0 + r.jj] * kBM;
-    r.a_row = r.jj * kBM;  // dZ rows are chunk-local
+    r.row0 = r.valid ? g.blk[g.chunk_b0 + r.jj] * kBM : N32;
+    // dZ rows are chunk-local; a missing partner reads past the chunk (zeros)
+    r.a_row = (r.valid ? r.jj : g.chunk_nb) * kBM;
   } else {
     // MODE_DW: output tile (vocab rows mt*128.., hidden columns t*bn..)
-    r.jj = u / g.n_nt;
-    r.t0 = u - r.jj * g.n_nt;
+    const int p = u / g.n_nt;
+    r.jj = PAIR ? 2 * p + rank : p;
+    r.valid = r.jj < g.n_mt;
+    r.t0 = u - p * g.n_nt;
     r.t1 = r.t0 + 1;
     r.side = 0;
     r.vs = 0;
-    r.row0 = r.jj * kBM;
+    r.row0 = r.jj * kBM;  // past V for a missing partner: zeros, nothing stored
     r.a_row = r.row0;
   }
   return r;
@@ -148,7 +185,7 @@ __device__ __forceinline__ float xform_logit(const GemmArgs& g, float z, float* 
   return u * g.x_inv_temp;
 }
 
-template <int MODE>
+template <int MODE, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
     k_gemm(const __grid_constant__ CUtensorMap mapA0, const __grid_constant__ CUtensorMap mapA1,
            const __grid_constant__ CUtensorMap mapB, const __grid_constant__ CUtensorMap mapC,
@@ -156,10 +193,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  constexpr int kStages = Cfg<PAIR>::kStages;
+  constexpr int kBStageBytes = Cfg<PAIR>::kBStageBytes;
   uint8_t* smA = smem;
   uint8_t* smB = smem + kStages * kAStageBytes;
   uint8_t* smOut = smB + kStages * kBStageBytes;  // 1024-byte aligned
   Smem* sh = reinterpret_cast<Smem*>(smOut + kOutBytes);
+  const int rank = PAIR ? static_cast<int>(cluster_ctarank()) : 0;
+  const bool leader = rank == 0;
+  const int unit0 = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  const int unit_stride = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -171,25 +214,37 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&sh->acc_full[b], 1);
-      mbar_init(&sh->acc_empty[b], kEpiThreads);
+      // PAIR: both CTAs' epilogues arrive on the even CTA's barrier
+      mbar_init(&sh->acc_empty[b], PAIR ? 2 * kEpiThreads : kEpiThreads);
     }
     mbar_init(&sh->mma_done, 1);
     sh->abort = 0;
     fence_barrier_init();
   }
   if (warp == 1) {
-    tmem_alloc(&sh->tmem_base, kTmemCols);
-    tmem_relinquish();
+    if (PAIR) {
+      tmem_alloc_pair(&sh->tmem_base, kTmemCols);  // with the peer CTA's warp 1
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(&sh->tmem_base, kTmemCols);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
-  __syncthreads();
+  if (PAIR)
+    cluster_sync();  // barrier inits and the allocation are visible to the peer
+  else
+    __syncthreads();
   tc_fence_after();
 
   const uint32_t tmem_base = sh->tmem_base;
   volatile int* abort = &sh->abort;
   const int nb = *g.nblk_dev;
-  const int n_units = unit_count<MODE>(g, nb);
-  const uint32_t b_bytes = static_cast<uint32_t>(g.bn) * kBK * 2;
+  const int n_units = unit_count<MODE, PAIR>(g, nb);
+  const int b_rows = PAIR ? g.bn >> 1 : g.bn;  // B rows this CTA loads per stage
+  const uint32_t b_bytes = static_cast<uint32_t>(b_rows) * kBK * 2;
+  // bytes the stage's full barrier waits for: both CTAs' loads for PAIR
+  const uint32_t tx_bytes = (PAIR ? 2u : 1u) * (kAStageBytes + b_bytes);
   // MODE_DW reduces over the chunk's tokens: two 64-wide K blocks per block
   const int nk = MODE == MODE_DW ? 2 * max(0, min(g.chunk_nb, nb - g.chunk_b0)) : g.nk;
   const int b_k0 = MODE == MODE_DW ? g.chunk_b0 * kBM : 0;  // B's K offset (H^T columns)
@@ -205,18 +260,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t issued = 0;           // stages that received at least one load
       uint32_t last_par = 0;         // parity bit of the last load per stage
       bool ok = true;
-      for (int u = blockIdx.x; ok && u < n_units; u += gridDim.x) {
-        const Unit un = unit_decode<MODE>(g, nb, u);
+      for (int u = unit0; ok && u < n_units; u += unit_stride) {
+        const Unit un = unit_decode<MODE, PAIR>(g, nb, u, rank);
         const CUtensorMap* mA = (MODE == MODE_FWD && un.side) ? &mapA1 : &mapA0;
         for (int t = un.t0; ok && t < un.t1; ++t) {
-          const int b_row = t * g.bn;
+          const int b_row = t * g.bn + rank * b_rows;
           for (int kb = 0; kb < nk; ++kb) {
-            if (!mbar_wait(&sh->empty[s], ph ^ 1u, abort, g.wait_ns)) {
+            const bool got = PAIR ? mbar_wait_cluster(&sh->empty[s], ph ^ 1u, abort, g.wait_ns)
+                                  : mbar_wait(&sh->empty[s], ph ^ 1u, abort, g.wait_ns);
+            if (!got) {
               ok = false;
               break;
             }
-            if (g.stall_test && blockIdx.x == 0 && u == static_cast<int>(blockIdx.x) &&
-                t == un.t0 && kb == 0) {
+            if (g.stall_test && blockIdx.x == 0 && u == unit0 && t == un.t0 && kb == 0) {
               // Testing: this stage is never armed, so the MMA warp's wait on
               // it expires and the CTA takes its abort path.
               if (++s == kStages) {
@@ -225,9 +281,15 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
               continue;
             }
-            mbar_arrive_expect_tx(&sh->full[s], kAStageBytes + b_bytes);
-            tma_load_2d(smA + s * kAStageBytes, mA, &sh->full[s], kb * kBK, un.a_row);
-            tma_load_2d(smB + s * kBStageBytes, &mapB, &sh->full[s], b_k0 + kb * kBK, b_row);
+            if (leader) mbar_arrive_expect_tx(&sh->full[s], tx_bytes);
+            if (PAIR) {
+              const uint32_t bar = mapa_shared(smem_u32(&sh->full[s]), 0);
+              tma_load_2d_pair(smA + s * kAStageBytes, mA, bar, kb * kBK, un.a_row);
+              tma_load_2d_pair(smB + s * kBStageBytes, &mapB, bar, b_k0 + kb * kBK, b_row);
+            } else {
+              tma_load_2d(smA + s * kAStageBytes, mA, &sh->full[s], kb * kBK, un.a_row);
+              tma_load_2d(smB + s * kBStageBytes, &mapB, &sh->full[s], b_k0 + kb * kBK, b_row);
+            }
             issued |= 1u << s;
             last_par = (last_par & ~(1u << s)) | (ph << s);
             if (++s == kStages) {
@@ -241,31 +303,39 @@ __global__ void __launch_bounds__(kThreads, 1)
         set_error(g.err, ERRBIT_TIMEOUT);
         *abort = 1;
       }
-      // Drain: every load issued must have landed before the CTA exits.
+      // Drain: every load issued must have landed before the CTA exits (for
+      // PAIR the even CTA's full barriers also count the odd CTA's loads).
       volatile int no_abort = 0;
-      for (int st = 0; st < kStages; ++st)
-        if (issued & (1u << st)) mbar_wait(&sh->full[st], (last_par >> st) & 1u, &no_abort, g.wait_ns);
+      if (leader)
+        for (int st = 0; st < kStages; ++st)
+          if (issued & (1u << st))
+            mbar_wait_cluster(&sh->full[st], (last_par >> st) & 1u, &no_abort, g.wait_ns);
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
-    if (lane == 0) {
-      const uint32_t idesc = idesc_bf16_f32(kBM, static_cast<uint32_t>(g.bn));
+    if (lane == 0 && leader) {
+      const uint32_t idesc = idesc_bf16_f32(PAIR ? 2 * kBM : kBM, static_cast<uint32_t>(g.bn));
       int s = 0;
       uint32_t ph = 0;
       int ab = 0;
       uint32_t aph = 0;
       bool ok = true;
-      for (int u = blockIdx.x; ok && u < n_units; u += gridDim.x) {
-        const Unit un = unit_decode<MODE>(g, nb, u);
+      for (int u = unit0; ok && u < n_units; u += unit_stride) {
+        const Unit un = unit_decode<MODE, PAIR>(g, nb, u, rank);
         for (int t = un.t0; ok && t < un.t1; ++t) {
-          if (!mbar_wait(&sh->acc_empty[ab], aph ^ 1u, abort, g.wait_ns)) {
+          const bool freed = PAIR
+                                 ? mbar_wait_cluster(&sh->acc_empty[ab], aph ^ 1u, abort, g.wait_ns)
+                                 : mbar_wait(&sh->acc_empty[ab], aph ^ 1u, abort, g.wait_ns);
+          if (!freed) {
             ok = false;
             break;
           }
           tc_fence_after();
           const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(ab * kAccStride);
           for (int kb = 0; kb < nk; ++kb) {
-            if (!mbar_wait(&sh->full[s], ph, abort, g.wait_ns)) {
+            const bool landed = PAIR ? mbar_wait_cluster(&sh->full[s], ph, abort, g.wait_ns)
+                                     : mbar_wait(&sh->full[s], ph, abort, g.wait_ns);
+            if (!landed) {
               ok = false;
               break;
             }
@@ -275,17 +345,27 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int k = 0; k < kBK / 16; ++k) {
               // K step of 16 elements: 32 bytes along the 128-byte swizzled rows
-              umma_bf16(d_tmem, sdesc_kmajor_sw128(a_addr + k * 32),
-                        sdesc_kmajor_sw128(b_addr + k * 32), idesc, (kb | k) != 0);
+              if (PAIR)
+                umma_bf16_pair(d_tmem, sdesc_kmajor_sw128(a_addr + k * 32),
+                               sdesc_kmajor_sw128(b_addr + k * 32), idesc, (kb | k) != 0);
+              else
+                umma_bf16(d_tmem, sdesc_kmajor_sw128(a_addr + k * 32),
+                          sdesc_kmajor_sw128(b_addr + k * 32), idesc, (kb | k) != 0);
             }
-            umma_commit(&sh->empty[s]);
+            if (PAIR)
+              umma_commit_pair(&sh->empty[s], 0x3);  // both CTAs' stage s is free
+            else
+              umma_commit(&sh->empty[s]);
             if (++s == kStages) {
               s = 0;
               ph ^= 1u;
             }
           }
           if (!ok) break;
-          umma_commit(&sh->acc_full[ab]);
+          if (PAIR)
+            umma_commit_pair(&sh->acc_full[ab], 0x3);
+          else
+            umma_commit(&sh->acc_full[ab]);
           if (++ab == 2) {
             ab = 0;
             aph ^= 1u;
@@ -297,7 +377,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         *abort = 1;
       }
       // Every MMA issued must complete before tensor memory is released.
-      umma_commit(&sh->mma_done);
+      if (PAIR)
+        umma_commit_pair(&sh->mma_done, 0x1);
+      else
+        umma_commit(&sh->mma_done);
       volatile int no_abort = 0;
       mbar_wait(&sh->mma_done, 0, &no_abort, g.wait_ns);
     }
@@ -313,10 +396,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     int ab = 0;
     uint32_t aph = 0;
     bool ok = true;
-    for (int u = blockIdx.x; ok && u < n_units; u += gridDim.x) {
-      const Unit un = unit_decode<MODE>(g, nb, u);
+    // PAIR: the accumulator-empty barrier that counts is the even CTA's
+    const uint32_t acc_empty_c0 = PAIR ? mapa_shared(smem_u32(&sh->acc_empty[0]), 0) : 0;
+    for (int u = unit0; ok && u < n_units; u += unit_stride) {
+      const Unit un = unit_decode<MODE, PAIR>(g, nb, u, rank);
       const int64_t row = static_cast<int64_t>(un.row0) + r_in_tile;
-      const bool in_range = row < (MODE == MODE_DW ? g.V : g.N);
+      const bool in_range = un.valid && row < (MODE == MODE_DW ? g.V : g.N);
 
       // per-unit state
       float m2 = -INFINITY, s_run = 0.f, s_comp = 0.f;  // FWD: running max / Kahan sum
@@ -338,7 +423,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       for (int t = un.t0; t < un.t1; ++t) {
         // warp-uniform outcome: the tensor-memory loads below are .sync.aligned
-        if (!__all_sync(0xffffffffu, mbar_wait(&sh->acc_full[ab], aph, abort, g.wait_ns))) {
+        const bool full = PAIR ? mbar_wait_cluster(&sh->acc_full[ab], aph, abort, g.wait_ns)
+                               : mbar_wait(&sh->acc_full[ab], aph, abort, g.wait_ns);
+        if (!__all_sync(0xffffffffu, full)) {
           ok = false;
           break;
         }
@@ -429,6 +516,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t pk[16];
 #pragma unroll
             for (int j = 0; j < 16; ++j) pk[j] = pack_bf16x2(o[2 * j], o[2 * j + 1]);
+            if (!un.valid) continue;  // a missing pair partner stores nothing
             // Stage the warp's 32 x 32 bf16 block in shared memory with the
             // 64-byte swizzle (16-byte piece v of row r lands at piece
             // v ^ ((r >> 1) & 3)), then one lane stores it with TMA; columns
@@ -524,14 +612,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         tc_fence_before();
-        mbar_arrive(&sh->acc_empty[ab]);
+        if (PAIR)
+          mbar_arrive_cluster(acc_empty_c0 + static_cast<uint32_t>(ab * sizeof(uint64_t)));
+        else
+          mbar_arrive(&sh->acc_empty[ab]);
         if (++ab == 2) {
           ab = 0;
           aph ^= 1u;
         }
       }
       if (!ok) break;
-      if (MODE == MODE_FWD) {
+      if (MODE == MODE_FWD && un.valid) {
         const int64_t pidx =
             (static_cast<int64_t>(un.side) * g.nblk_max + un.jj) * g.n_vs + un.vs;
         g.part[pidx * kBM + r_in_tile] = make_float2(m2, s_run);
@@ -546,45 +637,98 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   tc_fence_before();
-  __syncthreads();
+  // PAIR: neither CTA leaves while the other may still arrive on its barriers
+  if (PAIR)
+    cluster_sync();
+  else
+    __syncthreads();
   tc_fence_after();
   if (warp == 1) {
     __syncwarp();
-    tmem_dealloc(tmem_base, kTmemCols);
+    if (PAIR)
+      tmem_dealloc_pair(tmem_base, kTmemCols);
+    else
+      tmem_dealloc(tmem_base, kTmemCols);
   }
+}
+
+template <int MODE, bool PAIR>
+cudaError_t set_smem_limit() {
+  return cudaFuncSetAttribute(k_gemm<MODE, PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              Cfg<PAIR>::kSmemBytes);
+}
+
+template <int MODE, bool PAIR>
+cudaError_t launch_mode(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b,
+                        const CUtensorMap& c, const GemmArgs& args, int grid,
+                        cudaStream_t stream) {
+  if (!PAIR) {
+    k_gemm<MODE, false><<<grid, kThreads, Cfg<false>::kSmemBytes, stream>>>(a0, a1, b, c, args);
+    return cudaGetLastError();
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = Cfg<true>::kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k_gemm<MODE, true>, a0, a1, b, c, args);
 }
 
 }  // namespace
 
-size_t gemm_smem_bytes() { return kSmemBytes; }
+size_t gemm_smem_bytes() { return Cfg<false>::kSmemBytes; }
 
 cudaError_t gemm_configure() {
   cudaError_t e;
-  e = cudaFuncSetAttribute(k_gemm<MODE_FWD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           kSmemBytes);
-  if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(k_gemm<MODE_DZ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           kSmemBytes);
-  if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(k_gemm<MODE_DH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           kSmemBytes);
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(k_gemm<MODE_DW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              kSmemBytes);
+  if ((e = set_smem_limit<MODE_FWD, false>()) != cudaSuccess) return e;
+  if ((e = set_smem_limit<MODE_DZ, false>()) != cudaSuccess) return e;
+  if ((e = set_smem_limit<MODE_DH, false>()) != cudaSuccess) return e;
+  if ((e = set_smem_limit<MODE_DW, false>()) != cudaSuccess) return e;
+  if ((e = set_smem_limit<MODE_FWD, true>()) != cudaSuccess) return e;
+  if ((e = set_smem_limit<MODE_DZ, true>()) != cudaSuccess) return e;
+  if ((e = set_smem_limit<MODE_DH, true>()) != cudaSuccess) return e;
+  return set_smem_limit<MODE_DW, true>();
 }
 
-cudaError_t launch_gemm(int mode, const CUtensorMap& a0, const CUtensorMap& a1,
+int gemm_pair_clusters() {
+  // co-resident clusters of two CTAs for the pair kernels (same resources
+  // for every mode); 0 if the device cannot run them
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = Cfg<true>::kSmemBytes;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, k_gemm<MODE_FWD, true>, &cfg) != cudaSuccess) return 0;
+  return n;
+}
+
+cudaError_t launch_gemm(int mode, bool pair, const CUtensorMap& a0, const CUtensorMap& a1,
                         const CUtensorMap& b, const CUtensorMap& c, const GemmArgs& args,
                         int grid, cudaStream_t stream) {
-  if (mode == MODE_FWD)
-    k_gemm<MODE_FWD><<<grid, kThreads, kSmemBytes, stream>>>(a0, a1, b, c, args);
-  else if (mode == MODE_DZ)
-    k_gemm<MODE_DZ><<<grid, kThreads, kSmemBytes, stream>>>(a0, a1, b, c, args);
-  else if (mode == MODE_DH)
-    k_gemm<MODE_DH><<<grid, kThreads, kSmemBytes, stream>>>(a0, a1, b, c, args);
-  else
-    k_gemm<MODE_DW><<<grid, kThreads, kSmemBytes, stream>>>(a0, a1, b, c, args);
-  return cudaGetLastError();
+  if (pair) {
+    if (mode == MODE_FWD) return launch_mode<MODE_FWD, true>(a0, a1, b, c, args, grid, stream);
+    if (mode == MODE_DZ) return launch_mode<MODE_DZ, true>(a0, a1, b, c, args, grid, stream);
+    if (mode == MODE_DH) return launch_mode<MODE_DH, true>(a0, a1, b, c, args, grid, stream);
+    return launch_mode<MODE_DW, true>(a0, a1, b, c, args, grid, stream);
+  }
+  if (mode == MODE_FWD) return launch_mode<MODE_FWD, false>(a0, a1, b, c, args, grid, stream);
+  if (mode == MODE_DZ) return launch_mode<MODE_DZ, false>(a0, a1, b, c, args, grid, stream);
+  if (mode == MODE_DH) return launch_mode<MODE_DH, false>(a0, a1, b, c, args, grid, stream);
+  return launch_mode<MODE_DW, false>(a0, a1, b, c, args, grid, stream);
 }
 
 }  // namespace grpo

@@ -80,6 +80,7 @@ struct NvtxRange {
 struct DeviceInfo {
   int sms = 0;
   bool configured = false;
+  int pair_clusters = 0;  // co-resident CTA pairs of the cta_group::2 kernels
 };
 std::mutex g_dev_mu;
 DeviceInfo g_dev[64];
@@ -99,15 +100,29 @@ grpo_status device_info(int* sms) {
   return GRPO_OK;
 }
 
-grpo_status configure_kernels() {
+// Sets the kernels' shared-memory limits once per device and returns how
+// many CTA pairs of the cta_group::2 kernels can be resident at once.
+grpo_status configure_kernels(int* pair_clusters) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return GRPO_ERR_CUDA;
   std::lock_guard<std::mutex> lk(g_dev_mu);
   if (!g_dev[dev].configured) {
     if (gemm_configure() != cudaSuccess) return GRPO_ERR_CUDA;
+    g_dev[dev].pair_clusters = gemm_pair_clusters();
+    cudaGetLastError();  // a device without cluster support reports 0 pairs
     g_dev[dev].configured = true;
   }
+  *pair_clusters = g_dev[dev].pair_clusters;
   return GRPO_OK;
+}
+
+// GEMM grid: persistent CTAs, pairs of them when `pair`.
+int gemm_grid(bool pair, int sms, int pair_clusters, int64_t units_upper) {
+  if (pair) {
+    const int64_t pairs = units_upper < pair_clusters ? units_upper : pair_clusters;
+    return static_cast<int>(2 * (pairs > 0 ? pairs : 1));
+  }
+  return static_cast<int>(units_upper < sms ? (units_upper > 0 ? units_upper : 1) : sms);
 }
 
 // ------------------------------------------------------------- TMA maps
@@ -193,6 +208,7 @@ grpo_status validate_problem(const grpo_problem* p) {
   if (p->token_level != 0 && p->token_level != 1) return GRPO_ERR_INVALID_ARG;
   if (p->ref_logp_given != 0 && p->ref_logp_given != 1) return GRPO_ERR_INVALID_ARG;
   if (p->kl_mode < 0 || p->kl_mode > 3) return GRPO_ERR_INVALID_ARG;
+  if (p->cta_pairs != 0 && p->cta_pairs != 1) return GRPO_ERR_INVALID_ARG;
   for (float v : {p->logit_multiply, p->logit_divide, p->softcap, p->temperature})
     if (!isfinite(v) || v < 0.f) return GRPO_ERR_INVALID_ARG;
   return GRPO_OK;
@@ -405,8 +421,10 @@ grpo_status grpo_loss_fwd(const grpo_problem* problem, const void* H_pol, const 
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) % kAlign) != 0 ||
       workspace_bytes < P.f_total)
     return GRPO_ERR_WORKSPACE;
-  st = configure_kernels();
+  int pair_clusters = 0;
+  st = configure_kernels(&pair_clusters);
   if (st != GRPO_OK) return st;
+  const bool pair = problem->cta_pairs && pair_clusters > 0 && P.bn_dh >= 128;
 
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   Ctrl* ctrl = reinterpret_cast<Ctrl*>(ws);
@@ -438,7 +456,9 @@ grpo_status grpo_loss_fwd(const grpo_problem* problem, const void* H_pol, const 
   CUtensorMap mHp, mHr, mW;
   if ((st = make_map(&mHp, hp, P.d, P.N, P.d, kBM)) != GRPO_OK) return st;
   if ((st = make_map(&mHr, hr, P.d, P.N, P.d, kBM)) != GRPO_OK) return st;
-  if ((st = make_map(&mW, w, P.d, P.V, P.d, kVocabTile)) != GRPO_OK) return st;
+  // a CTA pair splits each 256-column vocab tile of W between its CTAs
+  if ((st = make_map(&mW, w, P.d, P.V, P.d, pair ? kVocabTile / 2 : kVocabTile)) != GRPO_OK)
+    return st;
 
   if (cudaMemsetAsync(ctrl, 0, sizeof(Ctrl), stream) != cudaSuccess) return GRPO_ERR_CUDA;
   LAUNCH(K_SEQ_COUNT, stream,
@@ -466,9 +486,10 @@ grpo_status grpo_loss_fwd(const grpo_problem* problem, const void* H_pol, const 
   set_xform(problem, &g);
   g.wait_ns = wait_limit_ns();
   g.stall_test = g_test.stall;
-  const int64_t units = static_cast<int64_t>(g.n_sides) * P.nblk_max * P.n_vs;
-  const int grid = static_cast<int>(units < P.sms ? units : P.sms);
-  LAUNCH(K_FWD_GEMM, stream, launch_gemm(MODE_FWD, mHp, mHr, mW, mW, g, grid, stream));
+  const int64_t units = static_cast<int64_t>(g.n_sides) *
+                        (pair ? (P.nblk_max + 1) / 2 : P.nblk_max) * P.n_vs;
+  const int grid = gemm_grid(pair, P.sms, pair_clusters, units);
+  LAUNCH(K_FWD_GEMM, stream, launch_gemm(MODE_FWD, pair, mHp, mHr, mW, mW, g, grid, stream));
 
   LAUNCH(K_FWD_FINISH, stream,
          launch_fwd_finish(inv, mask, cnt, adv, zy, part, P.nblk_max, P.n_vs, P.N, P.B, P.T,
@@ -500,8 +521,11 @@ grpo_status grpo_loss_bwd(const grpo_problem* problem, const void* H_pol, const 
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) % kAlign) != 0 ||
       workspace_bytes < P.b_total)
     return GRPO_ERR_WORKSPACE;
-  st = configure_kernels();
+  int pair_clusters = 0;
+  st = configure_kernels(&pair_clusters);
   if (st != GRPO_OK) return st;
+  const bool pair = problem->cta_pairs && pair_clusters > 0 && P.bn_dh >= 128;
+  const int bn_load = pair ? P.bn_dh / 2 : P.bn_dh;  // B rows of one CTA per tile
 
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   Ctrl* ctrl = reinterpret_cast<Ctrl*>(ws);
@@ -537,9 +561,10 @@ grpo_status grpo_loss_bwd(const grpo_problem* problem, const void* H_pol, const 
                          CU_TENSOR_MAP_SWIZZLE_64B)) != GRPO_OK)
     return st;
   if ((st = make_map(&mHp, hp, P.d, P.N, P.d, kBM)) != GRPO_OK) return st;
-  if ((st = make_map(&mW, w, P.d, P.V, P.d, kVocabTile)) != GRPO_OK) return st;
+  if ((st = make_map(&mW, w, P.d, P.V, P.d, pair ? kVocabTile / 2 : kVocabTile)) != GRPO_OK)
+    return st;
   if ((st = make_map(&mDz, dz, P.V, dz_rows, P.ldv, kBM)) != GRPO_OK) return st;
-  if ((st = make_map(&mWt, wt, P.V, P.d, P.ldv, P.bn_dh)) != GRPO_OK) return st;
+  if ((st = make_map(&mWt, wt, P.V, P.d, P.ldv, bn_load)) != GRPO_OK) return st;
   mDzTStore = mDzStore;  // placeholders when dW is off (not read)
   mDzT = mDz;
   mHt = mHp;
@@ -549,7 +574,7 @@ grpo_status grpo_loss_bwd(const grpo_problem* problem, const void* H_pol, const 
                            CU_TENSOR_MAP_SWIZZLE_64B)) != GRPO_OK)
       return st;
     if ((st = make_map(&mDzT, dzt, dz_rows, P.V, dz_rows, kBM)) != GRPO_OK) return st;
-    if ((st = make_map(&mHt, ht, ht_cols, P.d, ht_cols, P.bn_dh)) != GRPO_OK) return st;
+    if ((st = make_map(&mHt, ht, ht_cols, P.d, ht_cols, bn_load)) != GRPO_OK) return st;
   }
 
   if (cudaMemsetAsync(ctrl, 0, sizeof(Ctrl), stream) != cudaSuccess) return GRPO_ERR_CUDA;
@@ -602,27 +627,27 @@ grpo_status grpo_loss_bwd(const grpo_problem* problem, const void* H_pol, const 
   g.err = &ctrl->err;
   set_xform(problem, &g);
   g.wait_ns = wait_limit_ns();
-  const int64_t dz_units = static_cast<int64_t>(P.chunk_nb) * P.n_vt;
-  const int64_t dh_units = static_cast<int64_t>(P.chunk_nb) * P.n_nt;
-  const int grid_dz = static_cast<int>(dz_units < P.sms ? dz_units : P.sms);
-  const int grid_dh = static_cast<int>(dh_units < P.sms ? dh_units : P.sms);
-  const int64_t dw_units = static_cast<int64_t>(P.n_mt) * P.n_nt;
-  const int grid_dw = static_cast<int>(dw_units < P.sms ? dw_units : P.sms);
+  // units per launch (pairs of blocks for pair kernels)
+  const int64_t nbu = pair ? (P.chunk_nb + 1) / 2 : P.chunk_nb;
+  const int64_t nmu = pair ? (P.n_mt + 1) / 2 : P.n_mt;
+  const int grid_dz = gemm_grid(pair, P.sms, pair_clusters, nbu * P.n_vt);
+  const int grid_dh = gemm_grid(pair, P.sms, pair_clusters, nbu * P.n_nt);
+  const int grid_dw = gemm_grid(pair, P.sms, pair_clusters, nmu * P.n_nt);
   for (int c = 0; c < P.n_chunks; ++c) {
     NvtxRange nvtx_chunk("grpo_bwd_chunk");
     g.chunk_b0 = c * P.chunk_nb;
     GemmArgs gz = g;
     gz.bn = kVocabTile;
     gz.nk = P.nk_d;
-    LAUNCH(K_BWD_DZ_GEMM, stream, launch_gemm(MODE_DZ, mHp, mDzStore, mW, mDzTStore, gz, grid_dz, stream));
+    LAUNCH(K_BWD_DZ_GEMM, stream, launch_gemm(MODE_DZ, pair, mHp, mDzStore, mW, mDzTStore, gz, grid_dz, stream));
     GemmArgs gh = g;
     gh.bn = P.bn_dh;
     gh.nk = P.nk_v;
-    LAUNCH(K_BWD_DH_GEMM, stream, launch_gemm(MODE_DH, mDz, mDz, mWt, mDz, gh, grid_dh, stream));
+    LAUNCH(K_BWD_DH_GEMM, stream, launch_gemm(MODE_DH, pair, mDz, mDz, mWt, mDz, gh, grid_dh, stream));
     if (P.dw) {
       GemmArgs gw = g;
       gw.bn = P.bn_dh;
-      LAUNCH(K_BWD_DW_GEMM, stream, launch_gemm(MODE_DW, mDzT, mDzT, mHt, mDzT, gw, grid_dw, stream));
+      LAUNCH(K_BWD_DW_GEMM, stream, launch_gemm(MODE_DW, pair, mDzT, mDzT, mHt, mDzT, gw, grid_dw, stream));
     }
   }
   return GRPO_OK;
