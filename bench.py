@@ -294,7 +294,7 @@ def run_ours(args, w):
                      std_unbiased=w.std_unbiased, dtype=dt, device=dev, compute_dW=args.dW,
                      token_level=args.token_level, softcap=args.softcap,
                      temperature=args.temperature, ref_logp_given=args.ref_given,
-                     cta_pairs=args.cta_pairs)
+                     cluster_mode=args.cluster_mode)
     d_in = {k: (v.to(dev) if v is not None else None) for k, v in inp.items()}
     rewards = d_in["rewards"]
     adv_in = d_in["adv"]
@@ -436,7 +436,7 @@ def run_ours(args, w):
                        "variant": {"token_level": bool(args.token_level), "softcap": args.softcap,
                                    "temperature": args.temperature,
                                    "ref_logp_given": bool(args.ref_given),
-                                   "cta_pairs": bool(args.cta_pairs)},
+                                   "cluster_mode": args.cluster_mode},
                        "flops_per_step": fl["step"],
                        "parallelism": "replicas" if ws > 1 else "single",
                        "l2": "inputs larger than L2 (H_pol+H_ref+W = %.2f GB)"
@@ -485,8 +485,9 @@ def main():
     ap.add_argument("--token-level", action="store_true", help="token-level loss aggregation")
     ap.add_argument("--softcap", type=float, default=0.0, help="logit softcap (0 = off)")
     ap.add_argument("--temperature", type=float, default=0.0, help="logit temperature (0 = off)")
-    ap.add_argument("--cta-pairs", action="store_true",
-                    help="run the GEMMs on CTA pairs (tcgen05 cta_group::2)")
+    ap.add_argument("--cluster-mode", type=int, default=0, choices=[0, 1, 2],
+                    help="GEMM tiling: 0 one CTA per tile, 1 CTA pairs (cta_group::2), "
+                         "2 two-CTA clusters multicasting B")
     ap.add_argument("--ref-given", action="store_true",
                     help="reference log-probs supplied; skip the reference GEMM half")
     args = ap.parse_args()

@@ -34,11 +34,11 @@ class GRPOLoss:
                  compute_dW: bool = False, token_level: bool = False,
                  logit_multiply: float = 0.0, logit_divide: float = 0.0, softcap: float = 0.0,
                  temperature: float = 0.0, ref_logp_given: bool = False, kl_mode: int = 0,
-                 cta_pairs: bool = False):
+                 cluster_mode: int = 0):
         self.problem = make_problem(num_seqs, seq_len, d, V, group_size, beta, eps,
                                     std_unbiased, chunk_rows, dtype, compute_dW, token_level,
                                     logit_multiply, logit_divide, softcap, temperature,
-                                    ref_logp_given, kl_mode, cta_pairs)
+                                    ref_logp_given, kl_mode, cluster_mode)
         fwd_b, bwd_b = workspace_size(self.problem)
         dev = torch.device(device)
         self.ws_fwd = torch.empty(fwd_b, dtype=torch.uint8, device=dev)

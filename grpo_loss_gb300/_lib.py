@@ -40,7 +40,7 @@ class Problem(ctypes.Structure):
                 ("logit_multiply", ctypes.c_float), ("logit_divide", ctypes.c_float),
                 ("softcap", ctypes.c_float), ("temperature", ctypes.c_float),
                 ("ref_logp_given", ctypes.c_int32), ("kl_mode", ctypes.c_int32),
-                ("cta_pairs", ctypes.c_int32)]
+                ("cluster_mode", ctypes.c_int32)]
 
 
 def make_problem(num_seqs: int, seq_len: int, d: int, V: int, group_size: int,
@@ -49,7 +49,7 @@ def make_problem(num_seqs: int, seq_len: int, d: int, V: int, group_size: int,
                  token_level: bool = False, logit_multiply: float = 0.0,
                  logit_divide: float = 0.0, softcap: float = 0.0, temperature: float = 0.0,
                  ref_logp_given: bool = False, kl_mode: int = 0,
-                 cta_pairs: bool = False) -> Problem:
+                 cluster_mode: int = 0) -> Problem:
     return Problem(N=num_seqs * seq_len, d=d, V=V, num_seqs=num_seqs, seq_len=seq_len,
                    group_size=group_size, beta=beta, eps=eps, std_unbiased=std_unbiased,
                    chunk_rows=chunk_rows, compute_dW=1 if compute_dW else 0,
@@ -57,7 +57,7 @@ def make_problem(num_seqs: int, seq_len: int, d: int, V: int, group_size: int,
                    token_level=1 if token_level else 0, logit_multiply=logit_multiply,
                    logit_divide=logit_divide, softcap=softcap, temperature=temperature,
                    ref_logp_given=1 if ref_logp_given else 0, kl_mode=kl_mode,
-                   cta_pairs=1 if cta_pairs else 0)
+                   cluster_mode=cluster_mode)
 
 
 _lib = None

@@ -24,14 +24,19 @@
 // 256-column accumulators in tensor memory let the epilogue of one tile
 // overlap the MMAs of the next.
 //
-// PAIR = true runs CTA pairs (clusters of 2) on tcgen05 cta_group::2: a pair
+// KIND selects the tiling: KIND_SINGLE, one CTA per 128-row tile; KIND_PAIR,
+// CTA pairs (clusters of 2) on tcgen05 cta_group::2: a pair
 // computes a 256-row tile, each CTA holding its own 128 rows of A and half of
 // the B tile (6 stages of 32 KB instead of 4 of 48 KB). The even CTA arms the
 // full barrier for both CTAs' bytes (the odd CTA's TMA completes on it),
 // issues the MMAs and multicasts its commits to both CTAs; both CTAs'
 // epilogue threads arrive on the even CTA's accumulator-empty barrier. The
 // pair takes blocks 2p and 2p + 1; a missing partner block loads rows past
-// the end of its tensor (zeros) and writes nothing.
+// the end of its tensor (zeros) and writes nothing. KIND_MCAST keeps one CTA
+// per 128-row tile but clusters two CTAs whose tiles share B: each loads half
+// of the B tile and multicasts it into both CTAs' shared memory (a third less
+// L2 traffic), and each MMA warp multicasts its stage-consumed commit so a
+// stage is refilled only after both CTAs are done with it.
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -51,8 +56,11 @@ constexpr int kStageOutBytes = 32 * 64;
 constexpr int kOutBytes = 4 * 4 * kStageOutBytes;  // 32 KB
 constexpr float kLog2e = 1.4426950408889634f;
 
-template <bool PAIR>
+enum : int { KIND_SINGLE = 0, KIND_PAIR = 1, KIND_MCAST = 2 };
+
+template <int KIND>
 struct Cfg {
+  static constexpr bool PAIR = KIND == KIND_PAIR;
   static constexpr int kStages = PAIR ? 6 : 4;
   static constexpr int kBRows = PAIR ? 128 : 256;  // B rows of one CTA per stage (max)
   static constexpr int kBStageBytes = kBRows * kBK * 2;
@@ -82,34 +90,34 @@ struct Unit {
   bool valid;    // this CTA's block exists (false for a missing pair partner)
 };
 
-// Block counts seen by a unit: blocks, or block pairs for PAIR.
-template <bool PAIR>
+// Block counts seen by a unit: blocks, or block pairs for the clustered kinds.
+template <bool PAIRED>
 __device__ __forceinline__ int per_unit(int n) {
-  return PAIR ? (n + 1) >> 1 : n;
+  return PAIRED ? (n + 1) >> 1 : n;
 }
 
-template <int MODE, bool PAIR>
+template <int MODE, bool PAIRED>
 __device__ __forceinline__ int unit_count(const GemmArgs& g, int nb) {
-  if (MODE == MODE_FWD) return g.n_sides * per_unit<PAIR>(nb) * g.n_vs;
+  if (MODE == MODE_FWD) return g.n_sides * per_unit<PAIRED>(nb) * g.n_vs;
   const int nbc = min(g.chunk_nb, nb - g.chunk_b0);
   if (nbc <= 0) return 0;
-  if (MODE == MODE_DW) return per_unit<PAIR>(g.n_mt) * g.n_nt;
-  return MODE == MODE_DZ ? per_unit<PAIR>(nbc) * g.n_vt : per_unit<PAIR>(nbc) * g.n_nt;
+  if (MODE == MODE_DW) return per_unit<PAIRED>(g.n_mt) * g.n_nt;
+  return MODE == MODE_DZ ? per_unit<PAIRED>(nbc) * g.n_vt : per_unit<PAIRED>(nbc) * g.n_nt;
 }
 
-// `rank` is the CTA's place in its pair (0 without PAIR): it takes block
+// `rank` is the CTA's place in its cluster (0 when not PAIRED): it takes block
 // 2 p + rank of the unit's block pair p.
-template <int MODE, bool PAIR>
+template <int MODE, bool PAIRED>
 __device__ __forceinline__ Unit unit_decode(const GemmArgs& g, int nb, int u, int rank) {
   Unit r;
   const int N32 = static_cast<int>(g.N);  // a row past every tensor of rows: loads zeros
   if (MODE == MODE_FWD) {
-    const int nbp = per_unit<PAIR>(nb);
+    const int nbp = per_unit<PAIRED>(nb);
     const int i = u / g.n_vs;
     r.vs = u - i * g.n_vs;
     r.side = i >= nbp ? 1 : 0;
     const int p = i - r.side * nbp;
-    r.jj = PAIR ? 2 * p + rank : p;
+    r.jj = PAIRED ? 2 * p + rank : p;
     r.valid = r.jj < nb;
     r.row0 = r.valid ? g.blk[r.jj] * kBM : N32;
     r.a_row = r.row0;
@@ -117,8 +125,8 @@ __device__ __forceinline__ Unit unit_decode(const GemmArgs& g, int nb, int u, in
     r.t1 = static_cast<int>((static_cast<int64_t>(r.vs + 1) * g.n_vt) / g.n_vs);
   } else if (MODE == MODE_DZ) {
     const int nbc = min(g.chunk_nb, nb - g.chunk_b0);
-    const int nbcp = per_unit<PAIR>(nbc);
-    const int grp_sz = per_unit<PAIR>(g.group_blocks);
+    const int nbcp = per_unit<PAIRED>(nbc);
+    const int grp_sz = per_unit<PAIRED>(g.group_blocks);
     // groups of blocks walk the vocab tiles together, so each W tile is
     // fetched once per group while the group's A blocks stay in L2
     const int gsz_full = grp_sz * g.n_vt;
@@ -126,7 +134,7 @@ __device__ __forceinline__ Unit unit_decode(const GemmArgs& g, int nb, int u, in
     const int gb = min(grp_sz, nbcp - grp * grp_sz);
     const int rem = u - grp * gsz_full;
     const int p = grp * grp_sz + rem % gb;
-    r.jj = PAIR ? 2 * p + rank : p;
+    r.jj = PAIRED ? 2 * p + rank : p;
     r.valid = r.jj < nbc;
     r.t0 = rem / gb;
     r.t1 = r.t0 + 1;
@@ -139,11 +147,11 @@ __device__ __forceinline__ Unit unit_decode(const GemmArgs& g, int nb, int u, in
     // sms / nt_group blocks x nt_group column tiles, trading re-reads of the
     // dZ rows (once per group) against re-reads of W^T (once per wave)
     const int nbc = min(g.chunk_nb, nb - g.chunk_b0);
-    const int per_grp = per_unit<PAIR>(nbc) * g.nt_group;
+    const int per_grp = per_unit<PAIRED>(nbc) * g.nt_group;
     const int grp = u / per_grp;
     const int rem = u - grp * per_grp;
     const int p = rem / g.nt_group;
-    r.jj = PAIR ? 2 * p + rank : p;
+    r.jj = PAIRED ? 2 * p + rank : p;
     r.valid = r.jj < nbc;
     r.t0 = grp * g.nt_group + (rem - p * g.nt_group);
     r.t1 = r.t0 + 1;
@@ -155,7 +163,7 @@ __device__ __forceinline__ Unit unit_decode(const GemmArgs& g, int nb, int u, in
   } else {
     // MODE_DW: output tile (vocab rows mt*128.., hidden columns t*bn..)
     const int p = u / g.n_nt;
-    r.jj = PAIR ? 2 * p + rank : p;
+    r.jj = PAIRED ? 2 * p + rank : p;
     r.valid = r.jj < g.n_mt;
     r.t0 = u - p * g.n_nt;
     r.t1 = r.t0 + 1;
@@ -185,7 +193,7 @@ __device__ __forceinline__ float xform_logit(const GemmArgs& g, float z, float* 
   return u * g.x_inv_temp;
 }
 
-template <int MODE, bool PAIR>
+template <int MODE, int KIND>
 __global__ void __launch_bounds__(kThreads, 1)
     k_gemm(const __grid_constant__ CUtensorMap mapA0, const __grid_constant__ CUtensorMap mapA1,
            const __grid_constant__ CUtensorMap mapB, const __grid_constant__ CUtensorMap mapC,
@@ -193,16 +201,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  constexpr int kStages = Cfg<PAIR>::kStages;
-  constexpr int kBStageBytes = Cfg<PAIR>::kBStageBytes;
+  constexpr bool PAIR = KIND == KIND_PAIR;
+  constexpr bool MCAST = KIND == KIND_MCAST;
+  constexpr bool CLUSTER = KIND != KIND_SINGLE;  // units are block pairs
+  constexpr int kStages = Cfg<KIND>::kStages;
+  constexpr int kBStageBytes = Cfg<KIND>::kBStageBytes;
   uint8_t* smA = smem;
   uint8_t* smB = smem + kStages * kAStageBytes;
   uint8_t* smOut = smB + kStages * kBStageBytes;  // 1024-byte aligned
   Smem* sh = reinterpret_cast<Smem*>(smOut + kOutBytes);
-  const int rank = PAIR ? static_cast<int>(cluster_ctarank()) : 0;
-  const bool leader = rank == 0;
-  const int unit0 = PAIR ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
-  const int unit_stride = PAIR ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
+  const int rank = CLUSTER ? static_cast<int>(cluster_ctarank()) : 0;
+  const bool leader = PAIR ? rank == 0 : true;  // arms full barriers, issues MMAs
+  const int unit0 = CLUSTER ? static_cast<int>(blockIdx.x >> 1) : static_cast<int>(blockIdx.x);
+  const int unit_stride =
+      CLUSTER ? static_cast<int>(gridDim.x >> 1) : static_cast<int>(gridDim.x);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -210,7 +222,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&sh->full[s], 1);
-      mbar_init(&sh->empty[s], 1);
+      // MCAST: both CTAs' MMA warps release a stage (its B half came from each)
+      mbar_init(&sh->empty[s], MCAST ? 2 : 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&sh->acc_full[b], 1);
@@ -231,7 +244,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   tc_fence_before();
-  if (PAIR)
+  if (CLUSTER)
     cluster_sync();  // barrier inits and the allocation are visible to the peer
   else
     __syncthreads();
@@ -240,11 +253,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem_base = sh->tmem_base;
   volatile int* abort = &sh->abort;
   const int nb = *g.nblk_dev;
-  const int n_units = unit_count<MODE, PAIR>(g, nb);
-  const int b_rows = PAIR ? g.bn >> 1 : g.bn;  // B rows this CTA loads per stage
+  const int n_units = unit_count<MODE, CLUSTER>(g, nb);
+  const int b_rows = CLUSTER ? g.bn >> 1 : g.bn;  // B rows this CTA loads per stage
   const uint32_t b_bytes = static_cast<uint32_t>(b_rows) * kBK * 2;
-  // bytes the stage's full barrier waits for: both CTAs' loads for PAIR
-  const uint32_t tx_bytes = (PAIR ? 2u : 1u) * (kAStageBytes + b_bytes);
+  // bytes the stage's full barrier waits for: both CTAs' loads for PAIR; own
+  // A plus both multicast B halves for MCAST
+  const uint32_t tx_bytes = PAIR    ? 2u * (kAStageBytes + b_bytes)
+                            : MCAST ? kAStageBytes + 2u * b_bytes
+                                    : kAStageBytes + b_bytes;
   // MODE_DW reduces over the chunk's tokens: two 64-wide K blocks per block
   const int nk = MODE == MODE_DW ? 2 * max(0, min(g.chunk_nb, nb - g.chunk_b0)) : g.nk;
   const int b_k0 = MODE == MODE_DW ? g.chunk_b0 * kBM : 0;  // B's K offset (H^T columns)
@@ -261,13 +277,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t last_par = 0;         // parity bit of the last load per stage
       bool ok = true;
       for (int u = unit0; ok && u < n_units; u += unit_stride) {
-        const Unit un = unit_decode<MODE, PAIR>(g, nb, u, rank);
+        const Unit un = unit_decode<MODE, CLUSTER>(g, nb, u, rank);
         const CUtensorMap* mA = (MODE == MODE_FWD && un.side) ? &mapA1 : &mapA0;
         for (int t = un.t0; ok && t < un.t1; ++t) {
           const int b_row = t * g.bn + rank * b_rows;
           for (int kb = 0; kb < nk; ++kb) {
-            const bool got = PAIR ? mbar_wait_cluster(&sh->empty[s], ph ^ 1u, abort, g.wait_ns)
-                                  : mbar_wait(&sh->empty[s], ph ^ 1u, abort, g.wait_ns);
+            const bool got = CLUSTER
+                                 ? mbar_wait_cluster(&sh->empty[s], ph ^ 1u, abort, g.wait_ns)
+                                 : mbar_wait(&sh->empty[s], ph ^ 1u, abort, g.wait_ns);
             if (!got) {
               ok = false;
               break;
@@ -286,6 +303,11 @@ __global__ void __launch_bounds__(kThreads, 1)
               const uint32_t bar = mapa_shared(smem_u32(&sh->full[s]), 0);
               tma_load_2d_pair(smA + s * kAStageBytes, mA, bar, kb * kBK, un.a_row);
               tma_load_2d_pair(smB + s * kBStageBytes, &mapB, bar, b_k0 + kb * kBK, b_row);
+            } else if (MCAST) {
+              // own A; this CTA's half of the shared B tile, into both CTAs
+              tma_load_2d(smA + s * kAStageBytes, mA, &sh->full[s], kb * kBK, un.a_row);
+              tma_load_2d_mcast(smB + s * kBStageBytes + rank * b_bytes, &mapB, &sh->full[s],
+                                b_k0 + kb * kBK, b_row, 0x3);
             } else {
               tma_load_2d(smA + s * kAStageBytes, mA, &sh->full[s], kb * kBK, un.a_row);
               tma_load_2d(smB + s * kBStageBytes, &mapB, &sh->full[s], b_k0 + kb * kBK, b_row);
@@ -321,7 +343,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t aph = 0;
       bool ok = true;
       for (int u = unit0; ok && u < n_units; u += unit_stride) {
-        const Unit un = unit_decode<MODE, PAIR>(g, nb, u, rank);
+        const Unit un = unit_decode<MODE, CLUSTER>(g, nb, u, rank);
         for (int t = un.t0; ok && t < un.t1; ++t) {
           const bool freed = PAIR
                                  ? mbar_wait_cluster(&sh->acc_empty[ab], aph ^ 1u, abort, g.wait_ns)
@@ -333,8 +355,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(ab * kAccStride);
           for (int kb = 0; kb < nk; ++kb) {
-            const bool landed = PAIR ? mbar_wait_cluster(&sh->full[s], ph, abort, g.wait_ns)
-                                     : mbar_wait(&sh->full[s], ph, abort, g.wait_ns);
+            const bool landed = CLUSTER ? mbar_wait_cluster(&sh->full[s], ph, abort, g.wait_ns)
+                                        : mbar_wait(&sh->full[s], ph, abort, g.wait_ns);
             if (!landed) {
               ok = false;
               break;
@@ -354,6 +376,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (PAIR)
               umma_commit_pair(&sh->empty[s], 0x3);  // both CTAs' stage s is free
+            else if (MCAST)
+              umma_commit_mcast(&sh->empty[s], 0x3);  // this CTA is done with both halves
             else
               umma_commit(&sh->empty[s]);
             if (++s == kStages) {
@@ -399,7 +423,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // PAIR: the accumulator-empty barrier that counts is the even CTA's
     const uint32_t acc_empty_c0 = PAIR ? mapa_shared(smem_u32(&sh->acc_empty[0]), 0) : 0;
     for (int u = unit0; ok && u < n_units; u += unit_stride) {
-      const Unit un = unit_decode<MODE, PAIR>(g, nb, u, rank);
+      const Unit un = unit_decode<MODE, CLUSTER>(g, nb, u, rank);
       const int64_t row = static_cast<int64_t>(un.row0) + r_in_tile;
       const bool in_range = un.valid && row < (MODE == MODE_DW ? g.V : g.N);
 
@@ -423,8 +447,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       for (int t = un.t0; t < un.t1; ++t) {
         // warp-uniform outcome: the tensor-memory loads below are .sync.aligned
-        const bool full = PAIR ? mbar_wait_cluster(&sh->acc_full[ab], aph, abort, g.wait_ns)
-                               : mbar_wait(&sh->acc_full[ab], aph, abort, g.wait_ns);
+        const bool full = CLUSTER ? mbar_wait_cluster(&sh->acc_full[ab], aph, abort, g.wait_ns)
+                                  : mbar_wait(&sh->acc_full[ab], aph, abort, g.wait_ns);
         if (!__all_sync(0xffffffffu, full)) {
           ok = false;
           break;
@@ -637,8 +661,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   tc_fence_before();
-  // PAIR: neither CTA leaves while the other may still arrive on its barriers
-  if (PAIR)
+  // neither CTA of a cluster leaves while the other may still arrive on its
+  // barriers or write into its shared memory
+  if (CLUSTER)
     cluster_sync();
   else
     __syncthreads();
@@ -652,24 +677,25 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int MODE, bool PAIR>
+template <int MODE, int KIND>
 cudaError_t set_smem_limit() {
-  return cudaFuncSetAttribute(k_gemm<MODE, PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              Cfg<PAIR>::kSmemBytes);
+  return cudaFuncSetAttribute(k_gemm<MODE, KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              Cfg<KIND>::kSmemBytes);
 }
 
-template <int MODE, bool PAIR>
+template <int MODE, int KIND>
 cudaError_t launch_mode(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b,
                         const CUtensorMap& c, const GemmArgs& args, int grid,
                         cudaStream_t stream) {
-  if (!PAIR) {
-    k_gemm<MODE, false><<<grid, kThreads, Cfg<false>::kSmemBytes, stream>>>(a0, a1, b, c, args);
+  if (KIND == KIND_SINGLE) {
+    k_gemm<MODE, KIND_SINGLE><<<grid, kThreads, Cfg<KIND_SINGLE>::kSmemBytes, stream>>>(
+        a0, a1, b, c, args);
     return cudaGetLastError();
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = Cfg<true>::kSmemBytes;
+  cfg.dynamicSmemBytes = Cfg<KIND>::kSmemBytes;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -678,32 +704,36 @@ cudaError_t launch_mode(const CUtensorMap& a0, const CUtensorMap& a1, const CUte
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, k_gemm<MODE, true>, a0, a1, b, c, args);
+  return cudaLaunchKernelEx(&cfg, k_gemm<MODE, KIND>, a0, a1, b, c, args);
 }
 
 }  // namespace
 
-size_t gemm_smem_bytes() { return Cfg<false>::kSmemBytes; }
+size_t gemm_smem_bytes() { return Cfg<KIND_SINGLE>::kSmemBytes; }
+
+template <int KIND>
+cudaError_t configure_kind() {
+  cudaError_t e;
+  if ((e = set_smem_limit<MODE_FWD, KIND>()) != cudaSuccess) return e;
+  if ((e = set_smem_limit<MODE_DZ, KIND>()) != cudaSuccess) return e;
+  if ((e = set_smem_limit<MODE_DH, KIND>()) != cudaSuccess) return e;
+  return set_smem_limit<MODE_DW, KIND>();
+}
 
 cudaError_t gemm_configure() {
   cudaError_t e;
-  if ((e = set_smem_limit<MODE_FWD, false>()) != cudaSuccess) return e;
-  if ((e = set_smem_limit<MODE_DZ, false>()) != cudaSuccess) return e;
-  if ((e = set_smem_limit<MODE_DH, false>()) != cudaSuccess) return e;
-  if ((e = set_smem_limit<MODE_DW, false>()) != cudaSuccess) return e;
-  if ((e = set_smem_limit<MODE_FWD, true>()) != cudaSuccess) return e;
-  if ((e = set_smem_limit<MODE_DZ, true>()) != cudaSuccess) return e;
-  if ((e = set_smem_limit<MODE_DH, true>()) != cudaSuccess) return e;
-  return set_smem_limit<MODE_DW, true>();
+  if ((e = configure_kind<KIND_SINGLE>()) != cudaSuccess) return e;
+  if ((e = configure_kind<KIND_PAIR>()) != cudaSuccess) return e;
+  return configure_kind<KIND_MCAST>();
 }
 
 int gemm_pair_clusters() {
-  // co-resident clusters of two CTAs for the pair kernels (same resources
-  // for every mode); 0 if the device cannot run them
+  // co-resident clusters of two CTAs for the clustered kernels (the pair and
+  // multicast kernels use the same resources); 0 if the device cannot run them
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2, 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = Cfg<true>::kSmemBytes;
+  cfg.dynamicSmemBytes = Cfg<KIND_PAIR>::kSmemBytes;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
@@ -712,23 +742,27 @@ int gemm_pair_clusters() {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, k_gemm<MODE_FWD, true>, &cfg) != cudaSuccess) return 0;
+  if (cudaOccupancyMaxActiveClusters(&n, k_gemm<MODE_FWD, KIND_PAIR>, &cfg) != cudaSuccess)
+    return 0;
   return n;
 }
 
-cudaError_t launch_gemm(int mode, bool pair, const CUtensorMap& a0, const CUtensorMap& a1,
+template <int KIND>
+cudaError_t launch_kind(int mode, const CUtensorMap& a0, const CUtensorMap& a1,
                         const CUtensorMap& b, const CUtensorMap& c, const GemmArgs& args,
                         int grid, cudaStream_t stream) {
-  if (pair) {
-    if (mode == MODE_FWD) return launch_mode<MODE_FWD, true>(a0, a1, b, c, args, grid, stream);
-    if (mode == MODE_DZ) return launch_mode<MODE_DZ, true>(a0, a1, b, c, args, grid, stream);
-    if (mode == MODE_DH) return launch_mode<MODE_DH, true>(a0, a1, b, c, args, grid, stream);
-    return launch_mode<MODE_DW, true>(a0, a1, b, c, args, grid, stream);
-  }
-  if (mode == MODE_FWD) return launch_mode<MODE_FWD, false>(a0, a1, b, c, args, grid, stream);
-  if (mode == MODE_DZ) return launch_mode<MODE_DZ, false>(a0, a1, b, c, args, grid, stream);
-  if (mode == MODE_DH) return launch_mode<MODE_DH, false>(a0, a1, b, c, args, grid, stream);
-  return launch_mode<MODE_DW, false>(a0, a1, b, c, args, grid, stream);
+  if (mode == MODE_FWD) return launch_mode<MODE_FWD, KIND>(a0, a1, b, c, args, grid, stream);
+  if (mode == MODE_DZ) return launch_mode<MODE_DZ, KIND>(a0, a1, b, c, args, grid, stream);
+  if (mode == MODE_DH) return launch_mode<MODE_DH, KIND>(a0, a1, b, c, args, grid, stream);
+  return launch_mode<MODE_DW, KIND>(a0, a1, b, c, args, grid, stream);
+}
+
+cudaError_t launch_gemm(int mode, int kind, const CUtensorMap& a0, const CUtensorMap& a1,
+                        const CUtensorMap& b, const CUtensorMap& c, const GemmArgs& args,
+                        int grid, cudaStream_t stream) {
+  if (kind == KIND_PAIR) return launch_kind<KIND_PAIR>(mode, a0, a1, b, c, args, grid, stream);
+  if (kind == KIND_MCAST) return launch_kind<KIND_MCAST>(mode, a0, a1, b, c, args, grid, stream);
+  return launch_kind<KIND_SINGLE>(mode, a0, a1, b, c, args, grid, stream);
 }
 
 }  // namespace grpo

@@ -116,7 +116,7 @@ grpo_status configure_kernels(int* pair_clusters) {
   return GRPO_OK;
 }
 
-// GEMM grid: persistent CTAs, pairs of them when `pair`.
+// GEMM grid: persistent CTAs, in two-CTA clusters when `pair`.
 int gemm_grid(bool pair, int sms, int pair_clusters, int64_t units_upper) {
   if (pair) {
     const int64_t pairs = units_upper < pair_clusters ? units_upper : pair_clusters;
@@ -208,7 +208,7 @@ grpo_status validate_problem(const grpo_problem* p) {
   if (p->token_level != 0 && p->token_level != 1) return GRPO_ERR_INVALID_ARG;
   if (p->ref_logp_given != 0 && p->ref_logp_given != 1) return GRPO_ERR_INVALID_ARG;
   if (p->kl_mode < 0 || p->kl_mode > 3) return GRPO_ERR_INVALID_ARG;
-  if (p->cta_pairs != 0 && p->cta_pairs != 1) return GRPO_ERR_INVALID_ARG;
+  if (p->cluster_mode < 0 || p->cluster_mode > 2) return GRPO_ERR_INVALID_ARG;
   for (float v : {p->logit_multiply, p->logit_divide, p->softcap, p->temperature})
     if (!isfinite(v) || v < 0.f) return GRPO_ERR_INVALID_ARG;
   return GRPO_OK;
@@ -424,7 +424,10 @@ grpo_status grpo_loss_fwd(const grpo_problem* problem, const void* H_pol, const 
   int pair_clusters = 0;
   st = configure_kernels(&pair_clusters);
   if (st != GRPO_OK) return st;
-  const bool pair = problem->cta_pairs && pair_clusters > 0 && P.bn_dh >= 128;
+  // clustered kernels need resident two-CTA clusters and column tiles of at
+  // least 128 (halves of 64 rows or more)
+  const int kind = (pair_clusters > 0 && P.bn_dh >= 128) ? problem->cluster_mode : 0;
+  const bool pair = kind != 0;
 
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   Ctrl* ctrl = reinterpret_cast<Ctrl*>(ws);
@@ -489,7 +492,7 @@ grpo_status grpo_loss_fwd(const grpo_problem* problem, const void* H_pol, const 
   const int64_t units = static_cast<int64_t>(g.n_sides) *
                         (pair ? (P.nblk_max + 1) / 2 : P.nblk_max) * P.n_vs;
   const int grid = gemm_grid(pair, P.sms, pair_clusters, units);
-  LAUNCH(K_FWD_GEMM, stream, launch_gemm(MODE_FWD, pair, mHp, mHr, mW, mW, g, grid, stream));
+  LAUNCH(K_FWD_GEMM, stream, launch_gemm(MODE_FWD, kind, mHp, mHr, mW, mW, g, grid, stream));
 
   LAUNCH(K_FWD_FINISH, stream,
          launch_fwd_finish(inv, mask, cnt, adv, zy, part, P.nblk_max, P.n_vs, P.N, P.B, P.T,
@@ -524,7 +527,10 @@ grpo_status grpo_loss_bwd(const grpo_problem* problem, const void* H_pol, const 
   int pair_clusters = 0;
   st = configure_kernels(&pair_clusters);
   if (st != GRPO_OK) return st;
-  const bool pair = problem->cta_pairs && pair_clusters > 0 && P.bn_dh >= 128;
+  // clustered kernels need resident two-CTA clusters and column tiles of at
+  // least 128 (halves of 64 rows or more)
+  const int kind = (pair_clusters > 0 && P.bn_dh >= 128) ? problem->cluster_mode : 0;
+  const bool pair = kind != 0;
   const int bn_load = pair ? P.bn_dh / 2 : P.bn_dh;  // B rows of one CTA per tile
 
   uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -639,15 +645,15 @@ grpo_status grpo_loss_bwd(const grpo_problem* problem, const void* H_pol, const 
     GemmArgs gz = g;
     gz.bn = kVocabTile;
     gz.nk = P.nk_d;
-    LAUNCH(K_BWD_DZ_GEMM, stream, launch_gemm(MODE_DZ, pair, mHp, mDzStore, mW, mDzTStore, gz, grid_dz, stream));
+    LAUNCH(K_BWD_DZ_GEMM, stream, launch_gemm(MODE_DZ, kind, mHp, mDzStore, mW, mDzTStore, gz, grid_dz, stream));
     GemmArgs gh = g;
     gh.bn = P.bn_dh;
     gh.nk = P.nk_v;
-    LAUNCH(K_BWD_DH_GEMM, stream, launch_gemm(MODE_DH, pair, mDz, mDz, mWt, mDz, gh, grid_dh, stream));
+    LAUNCH(K_BWD_DH_GEMM, stream, launch_gemm(MODE_DH, kind, mDz, mDz, mWt, mDz, gh, grid_dh, stream));
     if (P.dw) {
       GemmArgs gw = g;
       gw.bn = P.bn_dh;
-      LAUNCH(K_BWD_DW_GEMM, stream, launch_gemm(MODE_DW, pair, mDzT, mDzT, mHt, mDzT, gw, grid_dw, stream));
+      LAUNCH(K_BWD_DW_GEMM, stream, launch_gemm(MODE_DW, kind, mDzT, mDzT, mHt, mDzT, gw, grid_dw, stream));
     }
   }
   return GRPO_OK;

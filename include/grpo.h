@@ -97,13 +97,14 @@ typedef struct grpo_problem {
                               detach (exp(q - q) * A: no gradient);
                            2: exp(q) * (exp(x) - x - 1) (the extra Q factor);
                            3: x exp(x) - exp(x) + 1 (forward KL under Q) */
-  int32_t cta_pairs;    /* 1: run the GEMMs on CTA pairs (tcgen05 cta_group::2,
-                           256-row tiles, half of each B tile per CTA) when the
-                           column tile is at least 128 wide; 0: one CTA per
-                           128-row tile. Pairs do more work per clock but draw
-                           more power: on a power-capped GB300 step they
-                           settled ~16% lower in clock and ran ~8% slower, so
-                           0 is the default. */
+  int32_t cluster_mode; /* GEMM tiling, when the column tile is at least 128
+                           wide: 0 one CTA per 128-row tile (default);
+                           1 CTA pairs on tcgen05 cta_group::2 (256-row tiles,
+                           half of each B tile per CTA); 2 two-CTA clusters
+                           that each load half of the shared B tile and
+                           multicast it to both. On a power-capped GB300 step
+                           mode 1 settled ~16% lower in clock and ran ~8%
+                           slower than mode 0. */
 } grpo_problem;
 
 /*

@@ -20,8 +20,8 @@ from tests.parity_util import TOL_REL, gpu_run, oracle_adv, rel_err
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("cta_pairs", [False, True], ids=["single", "pairs"])
-def test_pipeline_wait_timeout_is_reported_and_context_survives(cta_pairs):
+@pytest.mark.parametrize("cluster_mode", [0, 1, 2], ids=["single", "pairs", "multicast"])
+def test_pipeline_wait_timeout_is_reported_and_context_survives(cluster_mode):
     import grpo_loss_gb300 as G
     w = WL.SMALL["llama3.1-small"]
     inp = WL.make_inputs(w)
@@ -30,7 +30,7 @@ def test_pipeline_wait_timeout_is_reported_and_context_survives(cta_pairs):
     assert lib.grpo_test_pipeline_stall(1, 200) == 0
     try:
         t0 = time.time()
-        res = gpu_run(w, inp, adv32, want_bwd=False, check=False, cta_pairs=cta_pairs)
+        res = gpu_run(w, inp, adv32, want_bwd=False, check=False, cluster_mode=cluster_mode)
         status = G.device_status(res["engine"].ws_fwd)
         elapsed = time.time() - t0
     finally:
@@ -39,7 +39,7 @@ def test_pipeline_wait_timeout_is_reported_and_context_survives(cta_pairs):
     assert elapsed < 30.0
     assert G.device_status(res["engine"].ws_fwd) == 0   # read clears the word
     # the context is intact: a clean call matches the oracle
-    ok = gpu_run(w, inp, adv32, want_bwd=False, cta_pairs=cta_pairs)
+    ok = gpu_run(w, inp, adv32, want_bwd=False, cluster_mode=cluster_mode)
     f = O.forward(inp["H_pol"], inp["H_ref"], inp["W"], inp["ids"], inp["mask"], adv32.double(),
                   w.B, w.T, w.beta)
     m = inp["mask"].numpy() > 0

@@ -54,11 +54,17 @@ CASES = [
     ("kl-forward-token-softcap", WL.TINY, {"kl_mode": 3, "token_level": True, "softcap": 1.0}),
     # CTA-pair (cta_group::2) kernels: odd block counts leave a pair partner
     # without a block; d = 2880 pairs 96-row halves of 192-wide column tiles
-    ("pairs-llama", WL.SMALL["llama3.1-small"], {"cta_pairs": True}),
-    ("pairs-qwen3-odd-blocks", WL.SMALL["qwen3-small"], {"cta_pairs": True}),
-    ("pairs-tiny-all", WL.TINY, dict(XF, token_level=True, kl_mode=2, cta_pairs=True)),
+    ("pairs-llama", WL.SMALL["llama3.1-small"], {"cluster_mode": 1}),
+    ("pairs-qwen3-odd-blocks", WL.SMALL["qwen3-small"], {"cluster_mode": 1}),
+    ("pairs-tiny-all", WL.TINY, dict(XF, token_level=True, kl_mode=2, cluster_mode=1)),
     ("pairs-d2880", WL.GPTOSS_20B.scaled("gpt-oss-d2880", prompts=1, G=4, T=160, d=2880, V=2056,
-                                         pad_lo=80, pad_hi=160), {"cta_pairs": True}),
+                                         pad_lo=80, pad_hi=160), {"cluster_mode": 1}),
+    # two-CTA clusters multicasting the shared B halves
+    ("mcast-llama", WL.SMALL["llama3.1-small"], {"cluster_mode": 2}),
+    ("mcast-qwen3-odd-blocks", WL.SMALL["qwen3-small"], {"cluster_mode": 2}),
+    ("mcast-tiny-all", WL.TINY, dict(XF, token_level=True, kl_mode=3, cluster_mode=2)),
+    ("mcast-d2880", WL.GPTOSS_20B.scaled("gpt-oss-d2880", prompts=1, G=4, T=160, d=2880, V=2056,
+                                         pad_lo=80, pad_hi=160), {"cluster_mode": 2}),
 ]
 
 
