@@ -319,6 +319,25 @@ def run_ours(args, w):
     for _ in range(args.warmup):
         step(d_in)
     torch.cuda.synchronize()
+    timed_step = step
+    graph_launches_per_step = 0
+    if args.graph:
+        # kernels per step, counted on one eager step (a replay records none)
+        G.profile_enable(True)
+        G.profile_collect()
+        step(d_in)
+        torch.cuda.synchronize()
+        graph_launches_per_step = int(sum(v[1] for v in G.profile_collect().values()))
+        G.profile_enable(False)
+        # the whole step captured once and replayed (the library's calls are
+        # stream-ordered; the first call above set the kernel attributes)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            step(d_in)
+        timed_step = lambda _d: graph.replay()  # noqa: E731
+        for _ in range(args.warmup):
+            timed_step(d_in)
+        torch.cuda.synchronize()
     eng.check()
     if ws > 1:
         dist.barrier()
@@ -334,7 +353,7 @@ def run_ours(args, w):
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     ev0.record(stream)
     for _ in range(args.steps):
-        step(d_in)
+        timed_step(d_in)
     ev1.record(stream)
     torch.cuda.synchronize()
     if ws > 1:
@@ -415,12 +434,18 @@ def run_ours(args, w):
         fl = _flops(w, n_valid, args.dW, args.ref_given)
         gemms = {k: prof[k] for k in ("fwd_gemm_lse", "bwd_dz_gemm", "bwd_dh_gemm",
                                       "bwd_dw_gemm") if prof[k][1]}
-        dom = max(gemms, key=lambda k: gemms[k][0])
-        dom_ms, dom_launches = gemms[dom]
-        per_launch_flops = fl[dom] * args.steps / dom_launches
-        achieved = per_launch_flops / (dom_ms / dom_launches / 1e3) / 1e12
         peak = peaks["bf16_tflops_sustained"]
-        launches = int(sum(v[1] for v in prof.values()))
+        roofline = None
+        if gemms:  # (a replayed CUDA graph records no per-kernel events)
+            dom = max(gemms, key=lambda k: gemms[k][0])
+            dom_ms, dom_launches = gemms[dom]
+            per_launch_flops = fl[dom] * args.steps / dom_launches
+            achieved = per_launch_flops / (dom_ms / dom_launches / 1e3) / 1e12
+            roofline = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak,
+                        "unit": "TFLOP/s", "frac": achieved / peak,
+                        "traffic": measured_traffic(dom, w.name),
+                        "peak_kind": "bf16 sustained (%s)" % peaks["source"]}
+        launches = int(sum(v[1] for v in prof.values())) or graph_launches_per_step * args.steps
         kernels = {k: {"ms_per_step": v[0] / args.steps, "launches_per_step": v[1] / args.steps}
                    for k, v in prof.items() if v[1]}
         step_tflops = fl["step"] / (ms_step / 1e3) / 1e12
@@ -436,7 +461,8 @@ def run_ours(args, w):
                        "variant": {"token_level": bool(args.token_level), "softcap": args.softcap,
                                    "temperature": args.temperature,
                                    "ref_logp_given": bool(args.ref_given),
-                                   "cluster_mode": args.cluster_mode},
+                                   "cluster_mode": args.cluster_mode,
+                                   "cuda_graph": bool(args.graph)},
                        "flops_per_step": fl["step"],
                        "parallelism": "replicas" if ws > 1 else "single",
                        "l2": "inputs larger than L2 (H_pol+H_ref+W = %.2f GB)"
@@ -445,10 +471,7 @@ def run_ours(args, w):
             "tflops_per_step": step_tflops,
             "frac_of_peak": step_tflops / peak,
             "peak": {"bf16_tflops_sustained": peak, "source": peaks["source"]},
-            "roofline": {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak,
-                         "unit": "TFLOP/s", "frac": achieved / peak,
-                         "traffic": measured_traffic(dom, w.name),
-                         "peak_kind": "bf16 sustained (%s)" % peaks["source"]},
+            "roofline": roofline,
             "kernels": kernels,
             "memory": {
                 "fwd_workspace_bytes": eng.ws_fwd.numel(),
@@ -485,6 +508,8 @@ def main():
     ap.add_argument("--token-level", action="store_true", help="token-level loss aggregation")
     ap.add_argument("--softcap", type=float, default=0.0, help="logit softcap (0 = off)")
     ap.add_argument("--temperature", type=float, default=0.0, help="logit temperature (0 = off)")
+    ap.add_argument("--graph", action="store_true",
+                    help="time the step replayed from a CUDA graph")
     ap.add_argument("--cluster-mode", type=int, default=0, choices=[0, 1, 2],
                     help="GEMM tiling: 0 one CTA per tile, 1 CTA pairs (cta_group::2), "
                          "2 two-CTA clusters multicasting B")

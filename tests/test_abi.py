@@ -93,3 +93,29 @@ def test_profile_kinds(lib):
     names = [lib.grpo_profile_kind_name(k).decode() for k in range(n)]
     assert "fwd_gemm_lse" in names and "bwd_dh_gemm" in names and "bwd_dz_gemm" in names
     assert lib.grpo_profile_kind_name(n).decode() == "unknown"
+
+
+def test_problem_struct_layout_matches_the_header(tmp_path):
+    """The ctypes mirror of grpo_problem has the C header's field offsets and
+    size (compiled with the host C compiler against include/grpo.h)."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no host C compiler")
+    fields = [name for name, _ in L.Problem._fields_]
+    src = ["#include <stddef.h>", "#include <stdio.h>", '#include "grpo.h"', "int main(void) {",
+           '  printf("size %zu\\n", sizeof(grpo_problem));']
+    for f in fields:
+        src.append('  printf("%s %%zu\\n", offsetof(grpo_problem, %s));' % (f, f))
+    src += ["  return 0;", "}"]
+    c = tmp_path / "layout.c"
+    c.write_text("\n".join(src))
+    exe = tmp_path / "layout"
+    subprocess.run([cc, "-std=c11", "-I" + os.path.join(ROOT, "include"), str(c), "-o", str(exe)],
+                   check=True)
+    out = dict(line.split() for line in subprocess.run([str(exe)], capture_output=True,
+                                                       text=True, check=True).stdout.splitlines())
+    assert int(out["size"]) == ctypes.sizeof(L.Problem)
+    for f in fields:
+        assert int(out[f]) == getattr(L.Problem, f).offset, f
