@@ -108,3 +108,30 @@ def test_variant_sampled_rows_full_size(variant):
     assert rel_l2(res["dH"].numpy()[rows], g["dH"]) < TOL_DH_L2
     del res
     torch.cuda.empty_cache()
+
+
+def test_wide_vocab_softcap_head():
+    """A Gemma-3-shaped head (the pages list Gemma among the supported models,
+    and Gemma applies logit softcapping): V = 262144, d = 5376, softcap 30,
+    sampled rows against the oracle."""
+    w = WL.Workload("gemma3-shaped-head", prompts=1, G=4, T=512, d=5376, V=262144,
+                    mask="pad_uniform", pad_lo=384, pad_hi=512, rewards="normal", seed=1010)
+    inp = WL.make_inputs(w)
+    adv32 = torch.from_numpy(oracle_adv(w, inp)).float()
+    res = gpu_run(w, inp, adv32, softcap=30.0)
+    xf = {"softcap": 30.0}
+    rows = WL.sample_rows(w, inp["mask"], count=40)
+    m = inp["mask"].numpy()[rows] > 0
+    vrows = rows[m]
+    Wf = O.to_f64(inp["W"])
+    q, lse = O.token_logprobs(inp["H_pol"], Wf, inp["ids"], rows=vrows, xform=xf)
+    p, _ = O.token_logprobs(inp["H_ref"], Wf, inp["ids"], rows=vrows, xform=xf)
+    assert rel_err(res["logp_pol"].numpy()[vrows], q) < TOL_REL
+    assert rel_err(res["logp_ref"].numpy()[vrows], p) < TOL_REL
+    assert rel_err(res["lse_pol"].numpy()[vrows], lse) < TOL_REL
+    g = O.backward(inp["H_pol"], inp["H_ref"], Wf, inp["ids"], inp["mask"], adv32.double(),
+                   w.B, w.T, w.beta, rows=rows, xform=xf)
+    assert rel_l2(res["dH"].numpy()[rows][m], g["dH"][m]) < TOL_DH_L2
+    assert np.all(res["dH"].numpy()[rows][~m] == 0)
+    del res
+    torch.cuda.empty_cache()
