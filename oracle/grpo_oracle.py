@@ -60,6 +60,19 @@ Optional variants, all off by default:
 * Reference log-probabilities supplied by the caller instead of computed
   from H_ref (the reference model is frozen, so its log-probs can come from
   elsewhere, e.g. generation time).
+* FP8 operands. The pages name Float8 training only as a feature that
+  combines with the long-context loss (Unsloth "grpo-long-context" page, the
+  hint listing the features that combine, item 3) and warn that a naive
+  linear cross-entropy in float16 or float8 breaks mixed-precision scaling
+  (unsloth.ai GRPO blog, list of findings). They fix no format and no
+  scaling. The reading here: H_pol, H_ref and W are given as OCP FP8 E4M3
+  codes (the "fn" flavour: no infinities, S.1111.111 is NaN, largest finite
+  value 448) with one float32 scale per row, x = s * decode(q). The loss is
+  the same function of the dequantized operands, and dH and dW are its
+  gradients with respect to them. A row quantizer turns float32 or bf16 rows
+  into such codes: amax = max |x|, scale = amax / 448, codes =
+  round-to-nearest-even of x * (448 / amax), saturated to +-448, all in
+  float32 arithmetic.
 
 All inputs are taken at their exact values (bf16 and float32 upcast exactly to
 float64). Functions that take ``rows`` compute the listed rows only; every
@@ -75,7 +88,8 @@ import numpy as np
 __all__ = [
     "to_f64", "advantages", "sequence_weights", "token_logprobs", "kl_estimator",
     "forward", "loss_coefficients", "backward", "logit_memory_gib", "transform_logits",
-    "hidden_state_memory_gib",
+    "hidden_state_memory_gib", "e4m3_decode", "e4m3_encode", "quantize_e4m3_rows",
+    "dequantize_rows",
 ]
 
 
@@ -332,3 +346,73 @@ def logit_memory_gib(rows: int, vocab: int, multiplier: int = 1, bytes_per_elem:
 def hidden_state_memory_gib(batch: int, context: int, hidden: int) -> float:
     """Hidden-state footprint of the same page: batch * context * hidden / 1024^3."""
     return batch * context * hidden / 1024 ** 3
+
+
+# ---------------------------------------------------------------- FP8 E4M3
+
+E4M3_MAX = 448.0
+
+
+def e4m3_decode(codes) -> np.ndarray:
+    """Float64 values of E4M3 codes (uint8 array), from the format: sign bit,
+    4 exponent bits with bias 7, 3 mantissa bits; exponent field 0 holds the
+    subnormals m / 8 * 2^-6; exponent 15 with mantissa 7 is NaN (the format
+    has no infinities, so exponent 15 with mantissa 0..6 is an ordinary
+    binade reaching 448)."""
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    sign = np.where(c & 0x80, -1.0, 1.0)
+    e = (c >> 3) & 0xF
+    m = (c & 0x7).astype(np.float64)
+    mag = np.where(e == 0, m / 8.0 * 2.0 ** -6, (1.0 + m / 8.0) * np.exp2(e.astype(np.float64) - 7))
+    mag = np.where((e == 0xF) & (c & 0x7 == 0x7), np.nan, mag)
+    return sign * mag
+
+
+def e4m3_encode(x) -> np.ndarray:
+    """E4M3 codes of float32 values: round to the nearest representable value,
+    ties to the even code (the one whose last mantissa bit is 0), magnitudes
+    above 448 saturated to 448, NaN to 0x7F. A value that rounds to zero keeps
+    its sign (negative zero is 0x80)."""
+    x = np.asarray(x, dtype=np.float32)
+    a = np.abs(x).astype(np.float64)
+    table = e4m3_decode(np.arange(127, dtype=np.uint8))  # codes 0..126, increasing
+    hi = np.clip(np.searchsorted(table, a, side="left"), 0, 126)
+    lo = np.clip(hi - 1, 0, 126)
+    d_lo = a - table[lo]
+    d_hi = table[hi] - a
+    pick_hi = (d_hi < d_lo) | ((d_hi == d_lo) & (hi % 2 == 0))
+    code = np.where(pick_hi, hi, lo)
+    code = np.where(a >= E4M3_MAX, 126, code)
+    code = np.where(np.signbit(x), code | 0x80, code)
+    code = np.where(np.isnan(x), 0x7F, code)
+    return code.astype(np.uint8)
+
+
+def quantize_e4m3_rows(x):
+    """(codes uint8 [R, C], scales float32 [R]) of a float32 or bf16 matrix.
+
+    Per row in float32 arithmetic: amax = max |x|; scale = amax / 448 and
+    inv = 448 / amax (both correctly rounded divisions), or 1 and 1 for a row
+    of zeros; codes = e4m3_encode(x * inv) with one correctly rounded product
+    per element."""
+    if hasattr(x, "detach"):
+        x = x.detach().cpu().float().numpy()
+    x = np.asarray(x, dtype=np.float32)
+    amax = np.max(np.abs(x), axis=1) if x.shape[1] else np.zeros(x.shape[0], np.float32)
+    nz = amax > 0
+    safe = np.where(nz, amax, np.float32(1)).astype(np.float32)
+    scale = np.where(nz, safe / np.float32(E4M3_MAX), np.float32(1)).astype(np.float32)
+    inv = np.where(nz, np.float32(E4M3_MAX) / safe, np.float32(1)).astype(np.float32)
+    y = (x * inv[:, None]).astype(np.float32)
+    return e4m3_encode(y), scale
+
+
+def dequantize_rows(codes, scales) -> np.ndarray:
+    """Float64 [R, C] matrix s_r * decode(q_rc), the operand the e4m3 problem
+    is defined on (exact: the product of a 4-bit significand and a float32
+    scale fits in float64)."""
+    if hasattr(codes, "detach"):
+        codes = codes.detach().cpu().numpy()
+    if hasattr(scales, "detach"):
+        scales = scales.detach().cpu().numpy()
+    return e4m3_decode(codes) * np.asarray(scales, dtype=np.float64).reshape(-1, 1)

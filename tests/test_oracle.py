@@ -426,3 +426,71 @@ def test_kl_mode_estimators_vanish_at_equal_policies_and_are_nonnegative():
     # mode 3 small x: x^2/2 + x^3/3 + ...
     s = np.array([1e-3, -2e-3])
     assert np.allclose(O.kl_estimator(np.zeros(2), s, 3), s ** 2 / 2 + s ** 3 / 3, rtol=1e-5)
+
+
+# ------------------------------------------------------------------ FP8 E4M3
+
+def _torch_e4m3_codes(x32: np.ndarray) -> np.ndarray:
+    return torch.from_numpy(np.ascontiguousarray(x32)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+
+def test_e4m3_decode_matches_torch_float8_on_all_codes():
+    c = np.arange(256, dtype=np.uint8)
+    d = O.e4m3_decode(c)
+    t = torch.from_numpy(c).view(torch.float8_e4m3fn).double().numpy()
+    assert np.array_equal(np.isnan(d), np.isnan(t))
+    assert np.isnan(d).sum() == 2                      # 0x7F and 0xFF only
+    ok = ~np.isnan(d)
+    assert np.array_equal(d[ok], t[ok])
+    assert d[0x7E] == 448.0 and d[0x01] == 2.0 ** -9 and d[0x08] == 2.0 ** -6
+
+
+def test_e4m3_encode_matches_torch_cast_including_exact_ties():
+    g = np.random.default_rng(11)
+    mags = np.exp2(g.uniform(-12, np.log2(448.0), 20000))
+    x = (mags * g.choice([-1.0, 1.0], mags.size)).astype(np.float32)
+    # exact midpoints between neighbouring codes (ties go to the even code)
+    vals = O.e4m3_decode(np.arange(127, dtype=np.uint8))
+    mids = ((vals[:-1] + vals[1:]) / 2).astype(np.float32)
+    assert np.array_equal(mids.astype(np.float64), (vals[:-1] + vals[1:]) / 2)  # exact in f32
+    x = np.concatenate([x, mids, -mids, np.float32([0.0, -0.0, 1e-30, -1e-30, 448.0, -448.0])])
+    assert np.array_equal(O.e4m3_encode(x), _torch_e4m3_codes(x))
+
+
+def test_e4m3_encode_saturates_roundtrips_and_flags_nan():
+    x = np.float32([1000.0, -1e6, 449.0, 463.9, np.nan])
+    assert list(O.e4m3_encode(x)) == [0x7E, 0xFE, 0x7E, 0x7E, 0x7F]
+    c = np.array([k for k in range(256) if k not in (0x7F, 0xFF)], dtype=np.uint8)
+    again = O.e4m3_encode(O.e4m3_decode(c).astype(np.float32))
+    assert np.array_equal(O.e4m3_decode(again), O.e4m3_decode(c))
+    assert np.array_equal(again[c != 0x80], c[c != 0x80])
+
+
+def test_quantize_rows_hand_worked_row_and_zero_row():
+    # amax 4: scale 4/448 = 1/112, inv 112; scaled row 112, -224, 56, 448
+    # = 1.75 * 2^6, -1.75 * 2^7, 1.75 * 2^5, 1.75 * 2^8: exponent fields 13, 14,
+    # 12, 15 with mantissa 6
+    q, s = O.quantize_e4m3_rows(np.float32([[1.0, -2.0, 0.5, 4.0], [0.0, 0.0, 0.0, 0.0]]))
+    assert list(q[0]) == [0x6E, 0xF6, 0x66, 0x7E]
+    assert s[0] == np.float32(4.0) / np.float32(448.0)
+    assert list(q[1]) == [0, 0, 0, 0] and s[1] == 1.0
+    assert np.allclose(O.dequantize_rows(q[:1], s[:1]), [[1.0, -2.0, 0.5, 4.0]], rtol=1e-6)
+
+
+def test_quantize_rows_error_bound_and_dequantize_matches_torch():
+    g = torch.Generator().manual_seed(5)
+    x = (torch.randn(64, 300, generator=g) * torch.exp2(torch.randint(-20, 20, (64, 1), generator=g)))
+    x = x.to(torch.bfloat16)
+    q, s = O.quantize_e4m3_rows(x)
+    xf = x.double().numpy()
+    deq = O.dequantize_rows(q, s)
+    assert np.all(np.abs(O.e4m3_decode(q)).max(axis=1) == 448.0)
+    # normal codes: half a unit of 3 mantissa bits, 2^-4 relative (plus the
+    # float32 roundings of inv, scale and the product); subnormal codes: half
+    # their spacing 2^-9, in units of the row scale
+    y = np.abs(xf) * (448.0 / np.abs(xf).max(axis=1, keepdims=True))
+    bound = np.where(y >= 2.0 ** -6, np.abs(xf) * (2.0 ** -4 + 1e-6),
+                     2.0 ** -10 * s.astype(np.float64)[:, None] * (1 + 1e-6) + np.abs(xf) * 1e-6)
+    assert np.all(np.abs(deq - xf) <= bound)
+    t = torch.from_numpy(q).view(torch.float8_e4m3fn).double() * torch.from_numpy(s).double()[:, None]
+    assert np.array_equal(deq, t.numpy())
