@@ -11,12 +11,13 @@ from __future__ import annotations
 import torch
 
 from . import _lib
-from ._lib import (GrpoError, Problem, advantages, device_status, loss_bwd, loss_fwd,
-                   make_problem, profile_collect, profile_enable, workspace_size)
+from ._lib import (GrpoError, Problem, advantages, device_status, loss_bwd, loss_bwd_e4m3,
+                   loss_fwd, loss_fwd_e4m3, make_problem, profile_collect, profile_enable,
+                   quantize_e4m3_rows, workspace_size)
 
-__all__ = ["GrpoError", "Problem", "advantages", "device_status", "loss_bwd", "loss_fwd",
-           "make_problem", "profile_collect", "profile_enable", "workspace_size", "GRPOLoss",
-           "grpo_loss"]
+__all__ = ["GrpoError", "Problem", "advantages", "device_status", "loss_bwd", "loss_bwd_e4m3",
+           "loss_fwd", "loss_fwd_e4m3", "make_problem", "profile_collect", "profile_enable",
+           "quantize_e4m3_rows", "workspace_size", "GRPOLoss", "grpo_loss"]
 
 
 class GRPOLoss:
@@ -26,6 +27,12 @@ class GRPOLoss:
     ``backward`` returns dH_pol (and fills ``self.dW``, float32 [V, d], when
     built with ``compute_dW``). Buffers are allocated once with torch and
     reused across calls.
+
+    With ``dtype=torch.float8_e4m3fn`` the engine takes float32 or bf16 H_pol,
+    H_ref and W, quantizes them row-wise to e4m3 with the library's quantizer
+    and runs the e4m3 problem; dH is then bf16. The backward reuses the
+    forward's quantized H_pol and W while those tensors are unchanged (same
+    storage and version counter).
     """
 
     def __init__(self, num_seqs: int, seq_len: int, d: int, V: int, group_size: int,
@@ -53,6 +60,25 @@ class GRPOLoss:
         self.dtype = dtype
         self.dH = None
         self.dW = (torch.empty(V, d, dtype=torch.float32, device=dev) if compute_dW else None)
+        self.e4m3 = dtype == torch.float8_e4m3fn
+        if self.e4m3:
+            u8, f32 = torch.uint8, torch.float32
+            self.q_pol = torch.empty(N, d, dtype=u8, device=dev)
+            self.s_pol = torch.empty(N, dtype=f32, device=dev)
+            self.q_ref = None if ref_logp_given else torch.empty(N, d, dtype=u8, device=dev)
+            self.s_ref = None if ref_logp_given else torch.empty(N, dtype=f32, device=dev)
+            self.q_W = torch.empty(V, d, dtype=u8, device=dev)
+            self.s_W = torch.empty(V, dtype=f32, device=dev)
+            self._quantized = None  # (H_pol, W) identities the codes were made from
+
+    @staticmethod
+    def _ident(t):
+        return (t.data_ptr(), t._version, tuple(t.shape), t.dtype)
+
+    def _quantize(self, H_pol, W):
+        quantize_e4m3_rows(H_pol, self.q_pol, self.s_pol)
+        quantize_e4m3_rows(W, self.q_W, self.s_W)
+        self._quantized = (self._ident(H_pol), self._ident(W))
 
     def advantages(self, rewards: torch.Tensor) -> torch.Tensor:
         p = self.problem
@@ -65,17 +91,33 @@ class GRPOLoss:
             if logp_ref is None:
                 raise ValueError("ref_logp_given needs logp_ref")
             self.logp_ref.copy_(logp_ref)
-        loss_fwd(self.problem, H_pol, H_ref, W, ids, mask, adv, self.logp_pol, self.logp_ref,
-                 self.lse_pol, self.loss, self.kl_mean, self.ws_fwd)
+        if self.e4m3:
+            self._quantize(H_pol, W)
+            if H_ref is not None and self.q_ref is not None:
+                quantize_e4m3_rows(H_ref, self.q_ref, self.s_ref)
+            loss_fwd_e4m3(self.problem, self.q_pol, self.s_pol, self.q_ref, self.s_ref, self.q_W,
+                          self.s_W, ids, mask, adv, self.logp_pol, self.logp_ref, self.lse_pol,
+                          self.loss, self.kl_mean, self.ws_fwd)
+        else:
+            loss_fwd(self.problem, H_pol, H_ref, W, ids, mask, adv, self.logp_pol, self.logp_ref,
+                     self.lse_pol, self.loss, self.kl_mean, self.ws_fwd)
         return self.loss, self.kl_mean, self.logp_pol, self.logp_ref
 
     def backward(self, H_pol, W, ids, mask, adv, grad_loss: float = 1.0, dH=None):
         if dH is None:
             if self.dH is None:
-                self.dH = torch.empty_like(H_pol)
+                self.dH = (torch.empty(H_pol.shape, dtype=torch.bfloat16, device=H_pol.device)
+                           if self.e4m3 else torch.empty_like(H_pol))
             dH = self.dH
-        loss_bwd(self.problem, H_pol, W, ids, mask, adv, self.logp_pol, self.logp_ref,
-                 self.lse_pol, grad_loss, dH, self.ws_bwd, dW=self.dW)
+        if self.e4m3:
+            if self._quantized != (self._ident(H_pol), self._ident(W)):
+                self._quantize(H_pol, W)
+            loss_bwd_e4m3(self.problem, self.q_pol, self.s_pol, self.q_W, self.s_W, ids, mask,
+                          adv, self.logp_pol, self.logp_ref, self.lse_pol, grad_loss, dH,
+                          self.ws_bwd, dW=self.dW)
+        else:
+            loss_bwd(self.problem, H_pol, W, ids, mask, adv, self.logp_pol, self.logp_ref,
+                     self.lse_pol, grad_loss, dH, self.ws_bwd, dW=self.dW)
         return dH
 
     def check(self) -> None:
@@ -98,7 +140,11 @@ class _GRPOLossFn(torch.autograd.Function):
     def backward(ctx, g_loss, g_kl):
         H_pol, W, ids, mask, adv = ctx.saved_tensors
         # the upstream gradient is read on the host: one scalar per backward
-        dH = ctx.engine.backward(H_pol, W, ids, mask, adv, float(g_loss), dH=torch.empty_like(H_pol))
+        eng = ctx.engine
+        dH = eng.backward(H_pol, W, ids, mask, adv, float(g_loss),
+                          dH=torch.empty(H_pol.shape, dtype=torch.bfloat16, device=H_pol.device)
+                          if eng.e4m3 else torch.empty_like(H_pol))
+        dH = dH.to(H_pol.dtype)
         dW = ctx.engine.dW.to(W.dtype) if ctx.engine.dW is not None else None
         return dH, None, dW, None, None, None, None
 

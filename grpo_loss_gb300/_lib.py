@@ -19,7 +19,7 @@ GRPO_OK = 0
 STATUS_NAMES = {0: "GRPO_OK", 1: "GRPO_ERR_INVALID_ARG", 2: "GRPO_ERR_UNSUPPORTED",
                 3: "GRPO_ERR_WORKSPACE", 4: "GRPO_ERR_CUDA", 5: "GRPO_ERR_TIMEOUT",
                 6: "GRPO_ERR_BAD_TOKEN"}
-GRPO_F32, GRPO_BF16 = 0, 1
+GRPO_F32, GRPO_BF16, GRPO_E4M3 = 0, 1, 2
 
 
 class GrpoError(RuntimeError):
@@ -53,11 +53,23 @@ def make_problem(num_seqs: int, seq_len: int, d: int, V: int, group_size: int,
     return Problem(N=num_seqs * seq_len, d=d, V=V, num_seqs=num_seqs, seq_len=seq_len,
                    group_size=group_size, beta=beta, eps=eps, std_unbiased=std_unbiased,
                    chunk_rows=chunk_rows, compute_dW=1 if compute_dW else 0,
-                   dtype=GRPO_F32 if dtype == torch.float32 else GRPO_BF16,
+                   dtype=dtype_code(dtype),
                    token_level=1 if token_level else 0, logit_multiply=logit_multiply,
                    logit_divide=logit_divide, softcap=softcap, temperature=temperature,
                    ref_logp_given=1 if ref_logp_given else 0, kl_mode=kl_mode,
                    cluster_mode=cluster_mode)
+
+
+def dtype_code(dtype) -> int:
+    """grpo_dtype of a torch dtype: float32, bfloat16, or float8_e4m3fn for an
+    e4m3 problem (operands as codes with row scales)."""
+    if dtype == torch.float32:
+        return GRPO_F32
+    if dtype == torch.float8_e4m3fn:
+        return GRPO_E4M3
+    if dtype == torch.bfloat16:
+        return GRPO_BF16
+    raise ValueError("unsupported dtype %s" % (dtype,))
 
 
 _lib = None
@@ -73,6 +85,12 @@ _SIGNATURES = {
                       [_VP, ctypes.c_size_t, _VP]),
     "grpo_loss_bwd": (ctypes.c_int, [ctypes.POINTER(Problem)] + [_VP] * 8 +
                       [ctypes.c_float, _VP, _VP, _VP, ctypes.c_size_t, _VP]),
+    "grpo_loss_fwd_e4m3": (ctypes.c_int, [ctypes.POINTER(Problem)] + [_VP] * 14 +
+                           [_VP, ctypes.c_size_t, _VP]),
+    "grpo_loss_bwd_e4m3": (ctypes.c_int, [ctypes.POINTER(Problem)] + [_VP] * 10 +
+                           [ctypes.c_float, _VP, _VP, _VP, ctypes.c_size_t, _VP]),
+    "grpo_quantize_e4m3_rows": (ctypes.c_int, [_VP, ctypes.c_int, ctypes.c_int64, ctypes.c_int64,
+                                               _VP, _VP, _VP]),
     "grpo_get_device_status": (ctypes.c_int, [_VP, _VP]),
     "grpo_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "grpo_profile_enable": (ctypes.c_int, [ctypes.c_int32]),
@@ -173,6 +191,71 @@ def loss_bwd(problem: Problem, H_pol, W, ids, mask, adv, logp_pol, logp_ref, lse
         _ptr(dW, "dW", torch.float32, problem.V * problem.d),
         _ptr(workspace, "workspace"), workspace.numel() * workspace.element_size(),
         _stream(stream)), "grpo_loss_bwd")
+
+
+def _codes(t, name: str, numel: int):
+    """Pointer to e4m3 codes held as uint8 or float8_e4m3fn."""
+    if t is None:
+        return None
+    if t.dtype not in (torch.uint8, torch.float8_e4m3fn):
+        raise ValueError("%s must hold e4m3 codes (uint8 or float8_e4m3fn), got %s" % (name, t.dtype))
+    return _ptr(t, name, None, numel)
+
+
+def quantize_e4m3_rows(x: torch.Tensor, q=None, scale=None, stream=None):
+    """Row-wise e4m3 codes (uint8 [rows, cols]) and scales (float32 [rows]) of
+    a float32 or bf16 CUDA matrix; see grpo_quantize_e4m3_rows."""
+    if x.dim() != 2:
+        raise ValueError("x must be 2-D")
+    rows, cols = x.shape
+    if x.dtype == torch.float32:
+        code = GRPO_F32
+    elif x.dtype == torch.bfloat16:
+        code = GRPO_BF16
+    else:
+        raise ValueError("x must be float32 or bfloat16")
+    if q is None:
+        q = torch.empty(rows, cols, dtype=torch.uint8, device=x.device)
+    if scale is None:
+        scale = torch.empty(rows, dtype=torch.float32, device=x.device)
+    _check(lib().grpo_quantize_e4m3_rows(_ptr(x, "x"), code, rows, cols,
+                                         _codes(q, "q", rows * cols),
+                                         _ptr(scale, "scale", torch.float32, rows),
+                                         _stream(stream)), "grpo_quantize_e4m3_rows")
+    return q, scale
+
+
+def loss_fwd_e4m3(problem: Problem, H_pol, s_pol, H_ref, s_ref, W, s_W, ids, mask, adv,
+                  logp_pol, logp_ref, lse_pol, loss, kl_mean, workspace: torch.Tensor,
+                  stream=None) -> None:
+    N, Nd, Vd = problem.N, problem.N * problem.d, problem.V * problem.d
+    _check(lib().grpo_loss_fwd_e4m3(
+        ctypes.byref(problem), _codes(H_pol, "H_pol", Nd), _ptr(s_pol, "s_pol", torch.float32, N),
+        _codes(H_ref, "H_ref", Nd), _ptr(s_ref, "s_ref", torch.float32, N),
+        _codes(W, "W", Vd), _ptr(s_W, "s_W", torch.float32, problem.V),
+        _ptr(ids, "ids", torch.int32, N), _ptr(mask, "mask", torch.uint8, N),
+        _ptr(adv, "adv", torch.float32, problem.num_seqs),
+        _ptr(logp_pol, "logp_pol", torch.float32, N), _ptr(logp_ref, "logp_ref", torch.float32, N),
+        _ptr(lse_pol, "lse_pol", torch.float32, N), _ptr(loss, "loss", torch.float32, 1),
+        _ptr(kl_mean, "kl_mean", torch.float32, 1), _ptr(workspace, "workspace"),
+        workspace.numel() * workspace.element_size(), _stream(stream)), "grpo_loss_fwd_e4m3")
+
+
+def loss_bwd_e4m3(problem: Problem, H_pol, s_pol, W, s_W, ids, mask, adv, logp_pol, logp_ref,
+                  lse_pol, grad_loss: float, dH, workspace: torch.Tensor, stream=None,
+                  dW=None) -> None:
+    N, Nd, Vd = problem.N, problem.N * problem.d, problem.V * problem.d
+    _check(lib().grpo_loss_bwd_e4m3(
+        ctypes.byref(problem), _codes(H_pol, "H_pol", Nd), _ptr(s_pol, "s_pol", torch.float32, N),
+        _codes(W, "W", Vd), _ptr(s_W, "s_W", torch.float32, problem.V),
+        _ptr(ids, "ids", torch.int32, N), _ptr(mask, "mask", torch.uint8, N),
+        _ptr(adv, "adv", torch.float32, problem.num_seqs),
+        _ptr(logp_pol, "logp_pol", torch.float32, N), _ptr(logp_ref, "logp_ref", torch.float32, N),
+        _ptr(lse_pol, "lse_pol", torch.float32, N), float(grad_loss),
+        _ptr(dH, "dH", torch.bfloat16, Nd),
+        _ptr(dW, "dW", torch.float32, Vd),
+        _ptr(workspace, "workspace"), workspace.numel() * workspace.element_size(),
+        _stream(stream)), "grpo_loss_bwd_e4m3")
 
 
 def device_status(workspace: torch.Tensor, stream=None) -> int:

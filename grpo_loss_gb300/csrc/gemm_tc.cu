@@ -14,6 +14,11 @@
 //             epilogue) and H_pol^T, so both operands are K-major; the fp32
 //             result is accumulated into dW across chunks.
 //
+// MODE_FWD and MODE_DZ also take e4m3 operands (GemmArgs::fp8): the MMAs
+// are kind::f8f6f4, a 128-byte stage row holds 128 elements instead of 64,
+// and the epilogue multiplies each accumulator by the A row's and the B
+// row's scales before any other logit arithmetic.
+//
 // mapA1 is the reference hidden states in MODE_FWD and the store map of the
 // dZ chunk (32 x 32 boxes, 64-byte swizzle) in MODE_DZ; mapC is the store map
 // of dZ^T in MODE_DZ when dW is requested.
@@ -179,6 +184,30 @@ __device__ __forceinline__ void set_error(uint32_t* err, uint32_t bit) {
   if (err) atomicOr(err, bit);
 }
 
+// e4m3 operands: logits = acc * rs * sb[column] for the 32 columns from
+// col0 (rs the A row's scale, sb the scales of W's rows); columns at or past
+// V get 0, which no caller uses.
+__device__ __forceinline__ void apply_fp8_scales(uint32_t (&r)[32], float rs,
+                                                 const float* __restrict__ sb, int64_t col0,
+                                                 int64_t V) {
+  if (col0 + 32 <= V) {
+    const float4* s4 = reinterpret_cast<const float4*>(sb + col0);
+#pragma unroll
+    for (int v = 0; v < 8; ++v) {
+      const float4 sv = __ldg(s4 + v);
+      r[4 * v] = __float_as_uint(__uint_as_float(r[4 * v]) * rs * sv.x);
+      r[4 * v + 1] = __float_as_uint(__uint_as_float(r[4 * v + 1]) * rs * sv.y);
+      r[4 * v + 2] = __float_as_uint(__uint_as_float(r[4 * v + 2]) * rs * sv.z);
+      r[4 * v + 3] = __float_as_uint(__uint_as_float(r[4 * v + 3]) * rs * sv.w);
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      r[j] = __float_as_uint(col0 + j < V ? __uint_as_float(r[j]) * rs * __ldg(sb + col0 + j)
+                                          : 0.f);
+  }
+}
+
 // Optional logit transform z' = f(z): scale, then softcap, then temperature;
 // also returns f'(z) for the backward.
 __device__ __forceinline__ float xform_logit(const GemmArgs& g, float z, float* fprime) {
@@ -263,6 +292,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     : kAStageBytes + b_bytes;
   // MODE_DW reduces over the chunk's tokens: two 64-wide K blocks per block
   const int nk = MODE == MODE_DW ? 2 * max(0, min(g.chunk_nb, nb - g.chunk_b0)) : g.nk;
+  // e4m3 operands (logit GEMMs only): 128 elements per 128-byte stage row
+  const bool f8 = (MODE == MODE_FWD || MODE == MODE_DZ) && g.fp8 != 0;
+  const int kel = f8 ? 2 * kBK : kBK;
   const int b_k0 = MODE == MODE_DW ? g.chunk_b0 * kBM : 0;  // B's K offset (H^T columns)
 
   if (warp == 0) {
@@ -301,16 +333,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (leader) mbar_arrive_expect_tx(&sh->full[s], tx_bytes);
             if (PAIR) {
               const uint32_t bar = mapa_shared(smem_u32(&sh->full[s]), 0);
-              tma_load_2d_pair(smA + s * kAStageBytes, mA, bar, kb * kBK, un.a_row);
-              tma_load_2d_pair(smB + s * kBStageBytes, &mapB, bar, b_k0 + kb * kBK, b_row);
+              tma_load_2d_pair(smA + s * kAStageBytes, mA, bar, kb * kel, un.a_row);
+              tma_load_2d_pair(smB + s * kBStageBytes, &mapB, bar, b_k0 + kb * kel, b_row);
             } else if (MCAST) {
               // own A; this CTA's half of the shared B tile, into both CTAs
-              tma_load_2d(smA + s * kAStageBytes, mA, &sh->full[s], kb * kBK, un.a_row);
+              tma_load_2d(smA + s * kAStageBytes, mA, &sh->full[s], kb * kel, un.a_row);
               tma_load_2d_mcast(smB + s * kBStageBytes + rank * b_bytes, &mapB, &sh->full[s],
-                                b_k0 + kb * kBK, b_row, 0x3);
+                                b_k0 + kb * kel, b_row, 0x3);
             } else {
-              tma_load_2d(smA + s * kAStageBytes, mA, &sh->full[s], kb * kBK, un.a_row);
-              tma_load_2d(smB + s * kBStageBytes, &mapB, &sh->full[s], b_k0 + kb * kBK, b_row);
+              tma_load_2d(smA + s * kAStageBytes, mA, &sh->full[s], kb * kel, un.a_row);
+              tma_load_2d(smB + s * kBStageBytes, &mapB, &sh->full[s], b_k0 + kb * kel, b_row);
             }
             issued |= 1u << s;
             last_par = (last_par & ~(1u << s)) | (ph << s);
@@ -336,7 +368,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
     if (lane == 0 && leader) {
-      const uint32_t idesc = idesc_bf16_f32(PAIR ? 2 * kBM : kBM, static_cast<uint32_t>(g.bn));
+      const uint32_t idesc = f8 ? idesc_e4m3_f32(PAIR ? 2 * kBM : kBM, static_cast<uint32_t>(g.bn))
+                                : idesc_bf16_f32(PAIR ? 2 * kBM : kBM, static_cast<uint32_t>(g.bn));
       int s = 0;
       uint32_t ph = 0;
       int ab = 0;
@@ -366,13 +399,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t b_addr = smem_u32(smB + s * kBStageBytes);
 #pragma unroll
             for (int k = 0; k < kBK / 16; ++k) {
-              // K step of 16 elements: 32 bytes along the 128-byte swizzled rows
-              if (PAIR)
-                umma_bf16_pair(d_tmem, sdesc_kmajor_sw128(a_addr + k * 32),
-                               sdesc_kmajor_sw128(b_addr + k * 32), idesc, (kb | k) != 0);
-              else
-                umma_bf16(d_tmem, sdesc_kmajor_sw128(a_addr + k * 32),
-                          sdesc_kmajor_sw128(b_addr + k * 32), idesc, (kb | k) != 0);
+              // K step of 32 bytes along the 128-byte swizzled rows: 16 bf16 or
+              // 32 e4m3 elements
+              const uint64_t ad = sdesc_kmajor_sw128(a_addr + k * 32);
+              const uint64_t bd = sdesc_kmajor_sw128(b_addr + k * 32);
+              const uint32_t acc = (kb | k) != 0;
+              if (PAIR) {
+                if (f8)
+                  umma_e4m3_pair(d_tmem, ad, bd, idesc, acc);
+                else
+                  umma_bf16_pair(d_tmem, ad, bd, idesc, acc);
+              } else {
+                if (f8)
+                  umma_e4m3(d_tmem, ad, bd, idesc, acc);
+                else
+                  umma_bf16(d_tmem, ad, bd, idesc, acc);
+              }
             }
             if (PAIR)
               umma_commit_pair(&sh->empty[s], 0x3);  // both CTAs' stage s is free
@@ -432,6 +474,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       int32_t y = -1;
       float c_n = 0.f, lse2 = 0.f;
       bool live = false;
+      float rs = 1.f;  // e4m3: this row's scale
+      if (f8 && in_range) rs = (MODE == MODE_FWD && un.side) ? g.sa1[row] : g.sa0[row];
       if (MODE == MODE_FWD) {
         y = in_range ? g.ids[row] : -1;
       } else if (MODE == MODE_DZ) {
@@ -463,6 +507,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int c = 0; c < kVocabTile / 32; ++c) {
             uint32_t r[32];
             tmem_ld32_wait(tbase + c * 32, r);
+            if (f8) apply_fp8_scales(r, rs, g.sb, col_t + c * 32, g.V);
             if (g.xform) {  // uniform across the grid
               float fp;
 #pragma unroll
@@ -515,6 +560,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (col0 >= g.V) break;  // uniform across the warp
             uint32_t r[32];
             tmem_ld32_wait(tbase + c * 32, r);
+            if (f8) apply_fp8_scales(r, rs, g.sb, col0, g.V);
             float o[32];
             if (!g.xform) {
 #pragma unroll

@@ -38,7 +38,7 @@ constexpr size_t kMaxProfiled = 65536;
 const char* kKindNames[K_NUM_KINDS] = {
     "advantages", "convert_bf16", "seq_count",  "block_plan",  "fwd_gemm_lse", "fwd_finish",
     "fwd_reduce", "bwd_coef",     "transpose_w", "zero_rows",  "bwd_dz_gemm",  "bwd_dh_gemm",
-    "bwd_dw_gemm", "transpose_h"};
+    "bwd_dw_gemm", "transpose_h",  "quantize_e4m3"};
 
 void prof_begin(int k, cudaStream_t s) {
   if (!g_prof.on || g_prof.used >= kMaxProfiled) return;
@@ -145,17 +145,19 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// bf16 matrix [rows][inner] with row stride `ld` elements; box of
-// box_inner x box_rows elements with the given swizzle.
+// bf16 (or, with u8, one-byte) matrix [rows][inner] with row stride `ld`
+// elements; box of box_inner x box_rows elements with the given swizzle.
 grpo_status make_map_box(CUtensorMap* m, const void* base, int64_t inner, int64_t rows,
-                         int64_t ld, int box_inner, int box_rows, CUtensorMapSwizzle swz) {
+                         int64_t ld, int box_inner, int box_rows, CUtensorMapSwizzle swz,
+                         bool u8 = false) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return GRPO_ERR_CUDA;
   cuuint64_t gdim[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(rows)};
-  cuuint64_t gstride[1] = {static_cast<cuuint64_t>(ld) * 2};
+  cuuint64_t gstride[1] = {static_cast<cuuint64_t>(ld) * (u8 ? 1 : 2)};
   cuuint32_t box[2] = {static_cast<cuuint32_t>(box_inner), static_cast<cuuint32_t>(box_rows)};
   cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), gdim, gstride,
+  CUresult r = fn(m, u8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                  const_cast<void*>(base), gdim, gstride,
                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? GRPO_OK : GRPO_ERR_UNSUPPORTED;
@@ -166,6 +168,22 @@ grpo_status make_map_box(CUtensorMap* m, const void* base, int64_t inner, int64_
 grpo_status make_map(CUtensorMap* m, const void* base, int64_t inner, int64_t rows, int64_t ld,
                      int box_rows) {
   return make_map_box(m, base, inner, rows, ld, kBK, box_rows, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+// Operand map of an e4m3 matrix: box of 128 x box_rows one-byte elements
+// (the same 128-byte swizzled rows).
+grpo_status make_map_e4m3(CUtensorMap* m, const void* base, int64_t inner, int64_t rows,
+                          int64_t ld, int box_rows) {
+  return make_map_box(m, base, inner, rows, ld, 2 * kBK, box_rows, CU_TENSOR_MAP_SWIZZLE_128B,
+                      true);
+}
+
+// Operand map of H or W in the problem's element type (bf16 after any
+// float32 conversion, or e4m3).
+grpo_status make_operand_map(CUtensorMap* m, bool e4m3, const void* base, int64_t inner,
+                             int64_t rows, int64_t ld, int box_rows) {
+  return e4m3 ? make_map_e4m3(m, base, inner, rows, ld, box_rows)
+              : make_map(m, base, inner, rows, ld, box_rows);
 }
 
 // ------------------------------------------------------------------ plan
@@ -186,6 +204,7 @@ struct Plan {
   int n_chunks;
   int64_t ldv;       // padded row length of dZ and W^T
   bool f32;
+  bool e4m3;         // e4m3 operands with row scales
   // forward workspace offsets
   size_t f_cnt, f_blk, f_inv, f_zy, f_part, f_partials, f_hp16, f_hr16, f_w16, f_total;
   // backward workspace offsets
@@ -202,7 +221,10 @@ grpo_status validate_problem(const grpo_problem* p) {
     return GRPO_ERR_INVALID_ARG;
   if (p->d % 8 != 0 || p->d > 65536) return GRPO_ERR_UNSUPPORTED;
   if (!isfinite(p->beta) || !isfinite(p->eps)) return GRPO_ERR_INVALID_ARG;
-  if (p->dtype != GRPO_F32 && p->dtype != GRPO_BF16) return GRPO_ERR_INVALID_ARG;
+  if (p->dtype != GRPO_F32 && p->dtype != GRPO_BF16 && p->dtype != GRPO_E4M3)
+    return GRPO_ERR_INVALID_ARG;
+  // e4m3 rows are d bytes: TMA wants 16-byte row strides
+  if (p->dtype == GRPO_E4M3 && p->d % 16 != 0) return GRPO_ERR_UNSUPPORTED;
   if (p->chunk_rows < 0) return GRPO_ERR_INVALID_ARG;
   if (p->compute_dW != 0 && p->compute_dW != 1) return GRPO_ERR_INVALID_ARG;
   if (p->token_level != 0 && p->token_level != 1) return GRPO_ERR_INVALID_ARG;
@@ -239,6 +261,7 @@ grpo_status make_plan(const grpo_problem* p, Plan* pl) {
   P.G = p->group_size;
   P.sms = sms;
   P.f32 = p->dtype == GRPO_F32;
+  P.e4m3 = p->dtype == GRPO_E4M3;
   P.nblk_max = static_cast<int>(ceil_div(P.N, kBM));
   P.n_vt = static_cast<int>(ceil_div(P.V, kVocabTile));
   // Forward vocab slices. Units (side, block, slice) run slice-fastest, so
@@ -246,7 +269,7 @@ grpo_status make_plan(const grpo_problem* p, Plan* pl) {
   // their A blocks (128 x d bf16 each) within ~40 MB of L2, and add slices
   // only when that evens out the last wave of units noticeably.
   {
-    const double a_blk = 2.0 * kBM * static_cast<double>(P.d);
+    const double a_blk = (P.e4m3 ? 1.0 : 2.0) * kBM * static_cast<double>(P.d);
     int cb = static_cast<int>(kL2ABudget / a_blk);
     if (cb < 1) cb = 1;
     int vmin = static_cast<int>(ceil_div(sms, cb));
@@ -265,7 +288,7 @@ grpo_status make_plan(const grpo_problem* p, Plan* pl) {
         P.n_vs = v;
       }
   }
-  P.nk_d = static_cast<int>(ceil_div(P.d, kBK));
+  P.nk_d = static_cast<int>(ceil_div(P.d, P.e4m3 ? 2 * kBK : kBK));  // 128-byte K blocks
   P.nk_v = static_cast<int>(ceil_div(P.V, kBK));
   P.ldv = (P.V + 7) / 8 * 8;
   // widest tile over d (a multiple of 64, <= 256: dW reads H in 64-column
@@ -363,6 +386,19 @@ struct Ctrl {
   float kl_scratch;
 };
 
+grpo_status loss_fwd_impl(const grpo_problem* problem, const void* H_pol, const float* s_pol,
+                          const void* H_ref, const float* s_ref, const void* W,
+                          const float* s_W, const int32_t* ids, const uint8_t* mask,
+                          const float* adv, float* logp_pol, float* logp_ref, float* lse_pol,
+                          float* loss, float* kl_mean, void* workspace, size_t workspace_bytes,
+                          cudaStream_t stream);
+grpo_status loss_bwd_impl(const grpo_problem* problem, const void* H_pol, const float* s_pol,
+                          const void* W, const float* s_W, const int32_t* ids,
+                          const uint8_t* mask, const float* adv, const float* logp_pol,
+                          const float* logp_ref, const float* lse_pol, float grad_loss, void* dH,
+                          float* dW, void* workspace, size_t workspace_bytes,
+                          cudaStream_t stream);
+
 }  // namespace
 
 extern "C" {
@@ -408,13 +444,49 @@ grpo_status grpo_loss_fwd(const grpo_problem* problem, const void* H_pol, const 
                           float* loss, float* kl_mean, void* workspace, size_t workspace_bytes,
                           cudaStream_t stream) {
   NvtxRange nvtx_range("grpo_loss_fwd");
+  if (problem && problem->dtype == GRPO_E4M3) return GRPO_ERR_INVALID_ARG;
+  return loss_fwd_impl(problem, H_pol, nullptr, H_ref, nullptr, W, nullptr, ids, mask, adv,
+                       logp_pol, logp_ref, lse_pol, loss, kl_mean, workspace, workspace_bytes,
+                       stream);
+}
+
+grpo_status grpo_loss_fwd_e4m3(const grpo_problem* problem, const uint8_t* H_pol,
+                               const float* s_pol, const uint8_t* H_ref, const float* s_ref,
+                               const uint8_t* W, const float* s_W, const int32_t* ids,
+                               const uint8_t* mask, const float* adv, float* logp_pol,
+                               float* logp_ref, float* lse_pol, float* loss, float* kl_mean,
+                               void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  NvtxRange nvtx_range("grpo_loss_fwd_e4m3");
+  if (!problem || problem->dtype != GRPO_E4M3) return GRPO_ERR_INVALID_ARG;
+  const bool ref_given = problem->ref_logp_given != 0;
+  if (!s_pol || !s_W || (!s_ref && !ref_given)) return GRPO_ERR_INVALID_ARG;
+  if (!aligned16(s_W)) return GRPO_ERR_UNSUPPORTED;
+  return loss_fwd_impl(problem, H_pol, s_pol, H_ref, s_ref, W, s_W, ids, mask, adv, logp_pol,
+                       logp_ref, lse_pol, loss, kl_mean, workspace, workspace_bytes, stream);
+}
+
+}  // extern "C"
+
+namespace {
+
+// The forward of every element type; the row scales are used (and non-null)
+// for e4m3 problems only.
+grpo_status loss_fwd_impl(const grpo_problem* problem, const void* H_pol, const float* s_pol,
+                          const void* H_ref, const float* s_ref, const void* W,
+                          const float* s_W, const int32_t* ids, const uint8_t* mask,
+                          const float* adv, float* logp_pol, float* logp_ref, float* lse_pol,
+                          float* loss, float* kl_mean, void* workspace, size_t workspace_bytes,
+                          cudaStream_t stream) {
   grpo_status st = validate_problem(problem);
   if (st != GRPO_OK) return st;
   const bool ref_given = problem->ref_logp_given != 0;
   if (!H_pol || (!H_ref && !ref_given) || !W || !ids || !mask || !adv || !logp_pol ||
       !logp_ref || !lse_pol || !loss)
     return GRPO_ERR_INVALID_ARG;
-  if (ref_given) H_ref = H_pol;  // not read: only policy units are launched
+  if (ref_given) {
+    H_ref = H_pol;  // not read: only policy units are launched
+    s_ref = s_pol;
+  }
   Plan P;
   if ((st = make_plan(problem, &P)) != GRPO_OK) return st;
   if (!aligned16(H_pol) || !aligned16(H_ref) || !aligned16(W)) return GRPO_ERR_UNSUPPORTED;
@@ -457,10 +529,11 @@ grpo_status grpo_loss_fwd(const grpo_problem* problem, const void* H_pol, const 
   }
 
   CUtensorMap mHp, mHr, mW;
-  if ((st = make_map(&mHp, hp, P.d, P.N, P.d, kBM)) != GRPO_OK) return st;
-  if ((st = make_map(&mHr, hr, P.d, P.N, P.d, kBM)) != GRPO_OK) return st;
+  if ((st = make_operand_map(&mHp, P.e4m3, hp, P.d, P.N, P.d, kBM)) != GRPO_OK) return st;
+  if ((st = make_operand_map(&mHr, P.e4m3, hr, P.d, P.N, P.d, kBM)) != GRPO_OK) return st;
   // a CTA pair splits each 256-column vocab tile of W between its CTAs
-  if ((st = make_map(&mW, w, P.d, P.V, P.d, pair ? kVocabTile / 2 : kVocabTile)) != GRPO_OK)
+  if ((st = make_operand_map(&mW, P.e4m3, w, P.d, P.V, P.d,
+                             pair ? kVocabTile / 2 : kVocabTile)) != GRPO_OK)
     return st;
 
   if (cudaMemsetAsync(ctrl, 0, sizeof(Ctrl), stream) != cudaSuccess) return GRPO_ERR_CUDA;
@@ -489,6 +562,10 @@ grpo_status grpo_loss_fwd(const grpo_problem* problem, const void* H_pol, const 
   set_xform(problem, &g);
   g.wait_ns = wait_limit_ns();
   g.stall_test = g_test.stall;
+  g.fp8 = P.e4m3 ? 1 : 0;
+  g.sa0 = s_pol;
+  g.sa1 = s_ref;
+  g.sb = s_W;
   const int64_t units = static_cast<int64_t>(g.n_sides) *
                         (pair ? (P.nblk_max + 1) / 2 : P.nblk_max) * P.n_vs;
   const int grid = gemm_grid(pair, P.sms, pair_clusters, units);
@@ -505,12 +582,14 @@ grpo_status grpo_loss_fwd(const grpo_problem* problem, const void* H_pol, const 
   return GRPO_OK;
 }
 
-grpo_status grpo_loss_bwd(const grpo_problem* problem, const void* H_pol, const void* W,
-                          const int32_t* ids, const uint8_t* mask, const float* adv,
-                          const float* logp_pol, const float* logp_ref, const float* lse_pol,
-                          float grad_loss, void* dH, float* dW, void* workspace,
-                          size_t workspace_bytes, cudaStream_t stream) {
-  NvtxRange nvtx_range("grpo_loss_bwd");
+// The backward of every element type; the row scales are used (and
+// non-null) for e4m3 problems only.
+grpo_status loss_bwd_impl(const grpo_problem* problem, const void* H_pol, const float* s_pol,
+                          const void* W, const float* s_W, const int32_t* ids,
+                          const uint8_t* mask, const float* adv, const float* logp_pol,
+                          const float* logp_ref, const float* lse_pol, float grad_loss, void* dH,
+                          float* dW, void* workspace, size_t workspace_bytes,
+                          cudaStream_t stream) {
   grpo_status st = validate_problem(problem);
   if (st != GRPO_OK) return st;
   if (!H_pol || !W || !ids || !mask || !adv || !logp_pol || !logp_ref || !lse_pol || !dH)
@@ -566,8 +645,9 @@ grpo_status grpo_loss_bwd(const grpo_problem* problem, const void* H_pol, const 
   if ((st = make_map_box(&mDzStore, dz, P.V, dz_rows, P.ldv, 32, 32,
                          CU_TENSOR_MAP_SWIZZLE_64B)) != GRPO_OK)
     return st;
-  if ((st = make_map(&mHp, hp, P.d, P.N, P.d, kBM)) != GRPO_OK) return st;
-  if ((st = make_map(&mW, w, P.d, P.V, P.d, pair ? kVocabTile / 2 : kVocabTile)) != GRPO_OK)
+  if ((st = make_operand_map(&mHp, P.e4m3, hp, P.d, P.N, P.d, kBM)) != GRPO_OK) return st;
+  if ((st = make_operand_map(&mW, P.e4m3, w, P.d, P.V, P.d,
+                             pair ? kVocabTile / 2 : kVocabTile)) != GRPO_OK)
     return st;
   if ((st = make_map(&mDz, dz, P.V, dz_rows, P.ldv, kBM)) != GRPO_OK) return st;
   if ((st = make_map(&mWt, wt, P.V, P.d, P.ldv, bn_load)) != GRPO_OK) return st;
@@ -591,10 +671,12 @@ grpo_status grpo_loss_bwd(const grpo_problem* problem, const void* H_pol, const 
   LAUNCH(K_BWD_COEF, stream,
          launch_bwd_coef(mask, cnt, adv, logp_pol, logp_ref, P.N, P.B, P.T, problem->beta,
                          grad_loss, problem->token_level, problem->kl_mode, coef, stream));
-  LAUNCH(K_TRANSPOSE_W, stream, launch_transpose_w(W, P.f32, P.V, P.d, wt, P.ldv, stream));
+  const int w_type = P.f32 ? ELT_F32 : (P.e4m3 ? ELT_E4M3 : ELT_BF16);
+  LAUNCH(K_TRANSPOSE_W, stream,
+         launch_transpose_w(W, w_type, s_W, P.V, P.d, wt, P.ldv, stream));
   if (P.dw)
     LAUNCH(K_TRANSPOSE_H, stream,
-           launch_transpose_h_compact(static_cast<const __nv_bfloat16*>(hp), P.N, P.d, blk,
+           launch_transpose_h_compact(hp, P.e4m3 ? ELT_E4M3 : ELT_BF16, s_pol, P.N, P.d, blk,
                                       &ctrl->nblk, P.nblk_max, ht, ht_cols, stream));
   if (P.dw && cudaMemsetAsync(dW, 0, sizeof(float) * P.V * P.d, stream) != cudaSuccess)
     return GRPO_ERR_CUDA;
@@ -645,6 +727,9 @@ grpo_status grpo_loss_bwd(const grpo_problem* problem, const void* H_pol, const 
     GemmArgs gz = g;
     gz.bn = kVocabTile;
     gz.nk = P.nk_d;
+    gz.fp8 = P.e4m3 ? 1 : 0;
+    gz.sa0 = s_pol;
+    gz.sb = s_W;
     LAUNCH(K_BWD_DZ_GEMM, stream, launch_gemm(MODE_DZ, kind, mHp, mDzStore, mW, mDzTStore, gz, grid_dz, stream));
     GemmArgs gh = g;
     gh.bn = P.bn_dh;
@@ -656,6 +741,48 @@ grpo_status grpo_loss_bwd(const grpo_problem* problem, const void* H_pol, const 
       LAUNCH(K_BWD_DW_GEMM, stream, launch_gemm(MODE_DW, kind, mDzT, mDzT, mHt, mDzT, gw, grid_dw, stream));
     }
   }
+  return GRPO_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+grpo_status grpo_loss_bwd(const grpo_problem* problem, const void* H_pol, const void* W,
+                          const int32_t* ids, const uint8_t* mask, const float* adv,
+                          const float* logp_pol, const float* logp_ref, const float* lse_pol,
+                          float grad_loss, void* dH, float* dW, void* workspace,
+                          size_t workspace_bytes, cudaStream_t stream) {
+  NvtxRange nvtx_range("grpo_loss_bwd");
+  if (problem && problem->dtype == GRPO_E4M3) return GRPO_ERR_INVALID_ARG;
+  return loss_bwd_impl(problem, H_pol, nullptr, W, nullptr, ids, mask, adv, logp_pol, logp_ref,
+                       lse_pol, grad_loss, dH, dW, workspace, workspace_bytes, stream);
+}
+
+grpo_status grpo_loss_bwd_e4m3(const grpo_problem* problem, const uint8_t* H_pol,
+                               const float* s_pol, const uint8_t* W, const float* s_W,
+                               const int32_t* ids, const uint8_t* mask, const float* adv,
+                               const float* logp_pol, const float* logp_ref,
+                               const float* lse_pol, float grad_loss, void* dH, float* dW,
+                               void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  NvtxRange nvtx_range("grpo_loss_bwd_e4m3");
+  if (!problem || problem->dtype != GRPO_E4M3) return GRPO_ERR_INVALID_ARG;
+  if (!s_pol || !s_W) return GRPO_ERR_INVALID_ARG;
+  if (!aligned16(s_W)) return GRPO_ERR_UNSUPPORTED;
+  return loss_bwd_impl(problem, H_pol, s_pol, W, s_W, ids, mask, adv, logp_pol, logp_ref,
+                       lse_pol, grad_loss, dH, dW, workspace, workspace_bytes, stream);
+}
+
+grpo_status grpo_quantize_e4m3_rows(const void* x, grpo_dtype x_dtype, int64_t rows,
+                                    int64_t cols, uint8_t* q, float* scale,
+                                    cudaStream_t stream) {
+  NvtxRange nvtx_range("grpo_quantize_e4m3_rows");
+  if (!x || !q || !scale || rows < 0 || cols < 1) return GRPO_ERR_INVALID_ARG;
+  if (x_dtype != GRPO_F32 && x_dtype != GRPO_BF16) return GRPO_ERR_INVALID_ARG;
+  if (cols % 16 != 0 || !aligned16(x) || !aligned16(q) || !aligned16(scale))
+    return GRPO_ERR_UNSUPPORTED;
+  LAUNCH(K_QUANTIZE, stream,
+         launch_quantize_e4m3_rows(x, x_dtype == GRPO_F32 ? 1 : 0, rows, cols, q, scale, stream));
   return GRPO_OK;
 }
 

@@ -16,6 +16,9 @@ constexpr int kBM = 128;         // rows per output tile (one TMEM lane per row)
 constexpr int kBK = 64;          // bf16 K elements per 128-byte swizzled row
 constexpr int kVocabTile = 256;  // vocab columns per tile in the logit GEMMs
 
+// Element types of the operands a kernel reads.
+enum ElemType : int { ELT_BF16 = 0, ELT_F32 = 1, ELT_E4M3 = 2 };
+
 enum GemmMode : int { MODE_FWD = 0, MODE_DZ = 1, MODE_DH = 2, MODE_DW = 3 };
 
 // Everything a GEMM launch needs besides its tensor maps.
@@ -26,7 +29,7 @@ struct GemmArgs {
   int n_vt;               // vocab tiles of kVocabTile columns
   int n_nt;               // MODE_DH: output column tiles
   int bn;                 // output tile width (MODE_FWD/DZ: 256)
-  int nk;                 // 64-wide K blocks
+  int nk;                 // K blocks of 128 bytes (64 bf16 or 128 e4m3 elements)
   int chunk_b0;           // MODE_DZ/DH: first compacted block of the chunk
   int chunk_nb;           // MODE_DZ/DH: blocks per chunk
   int group_blocks;       // MODE_DZ: blocks per raster group
@@ -53,6 +56,11 @@ struct GemmArgs {
   uint32_t* err;          // device error word
   uint64_t wait_ns;       // pipeline wait limit
   int stall_test;         // testing: CTA 0 withholds its first stage (see grpo_test_pipeline_stall)
+  int fp8;                // MODE_FWD/MODE_DZ: e4m3 operands (kind::f8f6f4); logits are
+                          // acc * sa[row] * sb[column]
+  const float* sa0;       // row scales of A (policy rows)
+  const float* sa1;       // MODE_FWD: row scales of the reference rows
+  const float* sb;        // row scales of B (the vocab rows of W)
 };
 
 // Profiling kinds (one per kernel the library launches).
@@ -71,6 +79,7 @@ enum KernelKind : int {
   K_BWD_DH_GEMM,
   K_BWD_DW_GEMM,
   K_TRANSPOSE_H,
+  K_QUANTIZE,
   K_NUM_KINDS
 };
 
@@ -106,11 +115,16 @@ cudaError_t launch_bwd_coef(const uint8_t* mask, const int* cnt, const float* ad
                             const float* logp_pol, const float* logp_ref, int64_t N, int B,
                             int T, float beta, float grad, int token_level, int kl_mode,
                             float* coef, cudaStream_t s);
-cudaError_t launch_transpose_w(const void* W, int w_f32, int64_t V, int64_t d,
-                               __nv_bfloat16* Wt, int64_t ldwt, cudaStream_t s);
-cudaError_t launch_transpose_h_compact(const __nv_bfloat16* H, int64_t N, int64_t d,
-                                       const int* blk, const int* nblk_dev, int nblk_max,
-                                       __nv_bfloat16* Ht, int64_t ldht, cudaStream_t s);
+// W^T in bf16 from W of element type w_type (ELT_E4M3 rows times w_scale)
+cudaError_t launch_transpose_w(const void* W, int w_type, const float* w_scale, int64_t V,
+                               int64_t d, __nv_bfloat16* Wt, int64_t ldwt, cudaStream_t s);
+cudaError_t launch_transpose_h_compact(const void* H, int h_type, const float* h_scale,
+                                       int64_t N, int64_t d, const int* blk, const int* nblk_dev,
+                                       int nblk_max, __nv_bfloat16* Ht, int64_t ldht,
+                                       cudaStream_t s);
+// Row-wise e4m3 quantization of a float32 (x_f32) or bf16 matrix.
+cudaError_t launch_quantize_e4m3_rows(const void* x, int x_f32, int64_t rows, int64_t cols,
+                                      uint8_t* q, float* scale, cudaStream_t s);
 cudaError_t launch_zero_invalid_rows(const int* inv, int64_t N, int64_t d, void* out,
                                      int out_f32, cudaStream_t s);
 

@@ -242,6 +242,27 @@ __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint6
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// D[tmem] (+)= A[smem] * B[smem]^T for e4m3 A and B (kind::f8f6f4, K = 32
+// one-byte elements per instruction: 32 bytes of the swizzled rows, as for
+// bf16).
+__device__ __forceinline__ void umma_e4m3(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void umma_e4m3_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                               uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
 // Arrive once on `bar` when every tcgen05 op issued so far by this thread
 // has completed.
 __device__ __forceinline__ void umma_commit(uint64_t* bar) {
@@ -284,6 +305,16 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t M, uint32_t N, bo
          | (1u << 10)                 // B format bf16
          | ((a_mn ? 1u : 0u) << 15)   // A major-ness
          | ((b_mn ? 1u : 0u) << 16)   // B major-ness
+         | ((N >> 3) << 17)           // N / 8
+         | ((M >> 4) << 24);          // M / 16
+}
+
+// Instruction descriptor of kind::f8f6f4 with e4m3 A and B (format code 0
+// in both fields), f32 D, K-major operands, M x N tile.
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(uint32_t M, uint32_t N) {
+  return (1u << 4)                    // D format f32
+         | (0u << 7)                  // A format e4m3
+         | (0u << 10)                 // B format e4m3
          | ((N >> 3) << 17)           // N / 8
          | ((M >> 4) << 24);          // M / 16
 }

@@ -2,6 +2,8 @@
 // row plan (per-sequence counts and the list of 128-row blocks holding a
 // valid token), the per-token loss terms with deterministic float64
 // reductions, the backward coefficients, the W transpose and fills.
+#include <cuda_fp8.h>
+
 #include <algorithm>
 
 #include "internal.h"
@@ -319,22 +321,34 @@ __global__ void k_bwd_coef(const uint8_t* __restrict__ mask, const int* __restri
 }
 
 // ------------------------------------------------------------- transpose
-// Wt[c][r] = bf16(W[r][c]) for W [V, d] (bf16 or f32), 32x32 tiles.
-template <typename Tin>
-__global__ void k_transpose_w(const Tin* __restrict__ W, int64_t V, int64_t d,
-                              __nv_bfloat16* __restrict__ Wt, int64_t ldwt) {
+// One element of a matrix of element type ELT as float: bf16 and float32 as
+// stored; e4m3 decoded exactly and multiplied by its row's scale.
+template <int ELT>
+__device__ __forceinline__ float load_elt(const void* base, const float* row_scale, int64_t r,
+                                          int64_t i) {
+  if constexpr (ELT == ELT_F32) {
+    return static_cast<const float*>(base)[i];
+  } else if constexpr (ELT == ELT_BF16) {
+    return __bfloat162float(static_cast<const __nv_bfloat16*>(base)[i]);
+  } else {
+    __nv_fp8_e4m3 v;
+    v.__x = static_cast<const uint8_t*>(base)[i];
+    return static_cast<float>(v) * row_scale[r];
+  }
+}
+
+// Wt[c][r] = bf16(W[r][c]) for W [V, d], 32x32 tiles.
+template <int ELT>
+__global__ void k_transpose_w(const void* __restrict__ W, const float* __restrict__ w_scale,
+                              int64_t V, int64_t d, __nv_bfloat16* __restrict__ Wt,
+                              int64_t ldwt) {
   __shared__ float tile[32][33];
   const int64_t r0 = static_cast<int64_t>(blockIdx.x) * 32;
   const int64_t c0 = static_cast<int64_t>(blockIdx.y) * 32;
   for (int i = threadIdx.y; i < 32; i += blockDim.y) {
     const int64_t r = r0 + i, c = c0 + threadIdx.x;
     float v = 0.f;
-    if (r < V && c < d) {
-      if constexpr (sizeof(Tin) == 4)
-        v = W[r * d + c];
-      else
-        v = __bfloat162float(W[r * d + c]);
-    }
+    if (r < V && c < d) v = load_elt<ELT>(W, w_scale, r, r * d + c);
     tile[i][threadIdx.x] = v;
   }
   __syncthreads();
@@ -345,10 +359,12 @@ __global__ void k_transpose_w(const Tin* __restrict__ W, int64_t V, int64_t d,
 }
 
 // ----------------------------------------------------- compacted H^T
-// Ht[c][r] = H[src(r)][c] for compacted rows r in [0, nblk_max * 128): the
-// row of block blk[r / 128] at offset r % 128, or 0 past the valid blocks or
-// past N (those rows of dZ are 0, and 0 * garbage could be NaN).
-__global__ void k_transpose_h_compact(const __nv_bfloat16* __restrict__ H, int64_t N, int64_t d,
+// Ht[c][r] = bf16(H[src(r)][c]) for compacted rows r in [0, nblk_max * 128):
+// the row of block blk[r / 128] at offset r % 128, or 0 past the valid blocks
+// or past N (those rows of dZ are 0, and 0 * garbage could be NaN).
+template <int ELT>
+__global__ void k_transpose_h_compact(const void* __restrict__ H,
+                                      const float* __restrict__ h_scale, int64_t N, int64_t d,
                                       const int* __restrict__ blk, const int* nblk_dev,
                                       __nv_bfloat16* __restrict__ Ht, int64_t ldht) {
   __shared__ float tile[32][33];
@@ -361,7 +377,7 @@ __global__ void k_transpose_h_compact(const __nv_bfloat16* __restrict__ H, int64
     float v = 0.f;
     if (jb < nb && c < d) {
       const int64_t src = static_cast<int64_t>(blk[jb]) * kBM + (r - jb * kBM);
-      if (src < N) v = __bfloat162float(H[src * d + c]);
+      if (src < N) v = load_elt<ELT>(H, h_scale, src, src * d + c);
     }
     tile[i][threadIdx.x] = v;
   }
@@ -369,6 +385,75 @@ __global__ void k_transpose_h_compact(const __nv_bfloat16* __restrict__ H, int64
   for (int i = threadIdx.y; i < 32; i += blockDim.y) {
     const int64_t c = c0 + i, r = r0 + threadIdx.x;
     if (c < d) Ht[c * ldht + r] = __float2bfloat16_rn(tile[threadIdx.x][i]);
+  }
+}
+
+// ------------------------------------------------------ e4m3 quantization
+// One warp per row, 16 consecutive elements per lane step (cols % 16 == 0,
+// 16-byte aligned rows). amax = max |x| over the row; scale = amax / 448 and
+// inv = 448 / amax with correctly rounded divisions (1 and 1 for a row of
+// zeros); q = e4m3(x * inv), round to nearest even, saturated to +-448. The
+// row is read twice; the second pass mostly hits L1/L2.
+constexpr int kQuantRowsPerCta = 8;
+
+template <bool F32>
+__device__ __forceinline__ void load16(const void* x, int64_t e, float (&v)[16]) {
+  if constexpr (F32) {
+    const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(x) + e);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float4 f = p[k];
+      v[4 * k] = f.x;
+      v[4 * k + 1] = f.y;
+      v[4 * k + 2] = f.z;
+      v[4 * k + 3] = f.w;
+    }
+  } else {
+    const uint4* p = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(x) + e);
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const uint4 u = p[k];
+      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        v[8 * k + 2 * j] = __uint_as_float(w[j] << 16);
+        v[8 * k + 2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+      }
+    }
+  }
+}
+
+template <bool F32>
+__global__ void k_quantize_e4m3_rows(const void* __restrict__ x, int64_t rows, int64_t cols,
+                                     uint8_t* __restrict__ q, float* __restrict__ scale) {
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * kQuantRowsPerCta + warp;
+  if (row >= rows) return;
+  const int64_t ng = cols / 16;
+  const int64_t base = row * cols;
+  float amax = 0.f;
+  for (int64_t gi = lane; gi < ng; gi += 32) {
+    float v[16];
+    load16<F32>(x, base + gi * 16, v);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) amax = fmaxf(amax, fabsf(v[j]));
+  }
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  const bool nz = amax > 0.f;
+  const float inv = nz ? __fdiv_rn(448.f, amax) : 1.f;
+  if (lane == 0) scale[row] = nz ? __fdiv_rn(amax, 448.f) : 1.f;
+  for (int64_t gi = lane; gi < ng; gi += 32) {
+    float v[16];
+    load16<F32>(x, base + gi * 16, v);
+    uint32_t w[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const uint32_t b = __nv_cvt_float_to_fp8(__fmul_rn(v[j], inv), __NV_SATFINITE, __NV_E4M3);
+      w[j >> 2] |= (b & 0xFFu) << (8 * (j & 3));
+    }
+    *reinterpret_cast<uint4*>(q + base + gi * 16) = make_uint4(w[0], w[1], w[2], w[3]);
   }
 }
 
@@ -444,24 +529,42 @@ cudaError_t launch_bwd_coef(const uint8_t* mask, const int* cnt, const float* ad
   return cudaGetLastError();
 }
 
-cudaError_t launch_transpose_w(const void* W, int w_f32, int64_t V, int64_t d,
-                               __nv_bfloat16* Wt, int64_t ldwt, cudaStream_t s) {
+cudaError_t launch_transpose_w(const void* W, int w_type, const float* w_scale, int64_t V,
+                               int64_t d, __nv_bfloat16* Wt, int64_t ldwt, cudaStream_t s) {
   dim3 grid(static_cast<unsigned>((V + 31) / 32), static_cast<unsigned>((d + 31) / 32));
   dim3 block(32, 8);
-  if (w_f32)
-    k_transpose_w<float><<<grid, block, 0, s>>>(static_cast<const float*>(W), V, d, Wt, ldwt);
+  if (w_type == ELT_F32)
+    k_transpose_w<ELT_F32><<<grid, block, 0, s>>>(W, w_scale, V, d, Wt, ldwt);
+  else if (w_type == ELT_E4M3)
+    k_transpose_w<ELT_E4M3><<<grid, block, 0, s>>>(W, w_scale, V, d, Wt, ldwt);
   else
-    k_transpose_w<__nv_bfloat16>
-        <<<grid, block, 0, s>>>(static_cast<const __nv_bfloat16*>(W), V, d, Wt, ldwt);
+    k_transpose_w<ELT_BF16><<<grid, block, 0, s>>>(W, w_scale, V, d, Wt, ldwt);
   return cudaGetLastError();
 }
 
-cudaError_t launch_transpose_h_compact(const __nv_bfloat16* H, int64_t N, int64_t d,
-                                       const int* blk, const int* nblk_dev, int nblk_max,
-                                       __nv_bfloat16* Ht, int64_t ldht, cudaStream_t s) {
+cudaError_t launch_transpose_h_compact(const void* H, int h_type, const float* h_scale,
+                                       int64_t N, int64_t d, const int* blk, const int* nblk_dev,
+                                       int nblk_max, __nv_bfloat16* Ht, int64_t ldht,
+                                       cudaStream_t s) {
   dim3 grid(static_cast<unsigned>(nblk_max * (kBM / 32)), static_cast<unsigned>((d + 31) / 32));
   dim3 block(32, 8);
-  k_transpose_h_compact<<<grid, block, 0, s>>>(H, N, d, blk, nblk_dev, Ht, ldht);
+  if (h_type == ELT_E4M3)
+    k_transpose_h_compact<ELT_E4M3>
+        <<<grid, block, 0, s>>>(H, h_scale, N, d, blk, nblk_dev, Ht, ldht);
+  else
+    k_transpose_h_compact<ELT_BF16>
+        <<<grid, block, 0, s>>>(H, h_scale, N, d, blk, nblk_dev, Ht, ldht);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_e4m3_rows(const void* x, int x_f32, int64_t rows, int64_t cols,
+                                      uint8_t* q, float* scale, cudaStream_t s) {
+  if (rows <= 0) return cudaSuccess;
+  const unsigned grid = static_cast<unsigned>((rows + kQuantRowsPerCta - 1) / kQuantRowsPerCta);
+  if (x_f32)
+    k_quantize_e4m3_rows<true><<<grid, 32 * kQuantRowsPerCta, 0, s>>>(x, rows, cols, q, scale);
+  else
+    k_quantize_e4m3_rows<false><<<grid, 32 * kQuantRowsPerCta, 0, s>>>(x, rows, cols, q, scale);
   return cudaGetLastError();
 }
 

@@ -193,3 +193,25 @@ def sample_rows(w: Workload, mask: torch.Tensor, count: int, seed: int = 7) -> n
     while len(rows) < count and len(rows) < w.N:
         rows.add(int(rng.integers(0, w.N)))
     return np.array(sorted(rows), dtype=np.int64)
+
+
+def random_e4m3_operands(w: Workload, seed: int = 0) -> Dict[str, torch.Tensor]:
+    """E4M3 codes and float32 row scales drawn directly (no quantization):
+    codes uniform over the 254 non-NaN bytes (every sign, exponent and
+    mantissa pattern, subnormals included), scales 2^U(-1, 1) times a base
+    that puts the logits near unit scale. Keys q_pol, s_pol, q_ref, s_ref,
+    q_W, s_W (host tensors)."""
+    gen = torch.Generator().manual_seed(w.seed * 7919 + seed)
+    pool = torch.tensor([c for c in range(256) if c not in (0x7F, 0xFF)], dtype=torch.uint8)
+    # E[decode(code)^2] over that pool is about 1.0e4; z = s_h s_w sum_k q_h q_w
+    # has a standard deviation near s_h s_w sqrt(d) 1.0e4, so s ~ (sqrt(d) 1.0e4)^-1/2
+    base = float((np.sqrt(w.d) * 1.0e4) ** -0.5)
+
+    def codes(rows):
+        return pool[torch.randint(0, pool.numel(), (rows, w.d), generator=gen)]
+
+    def scales(rows):
+        return (base * torch.exp2(torch.rand(rows, generator=gen) * 2 - 1)).float()
+
+    return {"q_pol": codes(w.N), "s_pol": scales(w.N), "q_ref": codes(w.N), "s_ref": scales(w.N),
+            "q_W": codes(w.V), "s_W": scales(w.V)}

@@ -60,12 +60,14 @@ typedef enum grpo_status {
 } grpo_status;
 
 /* Element type of H_pol, H_ref, W and dH. GRPO_F32 inputs are rounded to
- * bf16 for the tensor-core products; accumulation is float32 either way. */
-typedef enum grpo_dtype { GRPO_F32 = 0, GRPO_BF16 = 1 } grpo_dtype;
+ * bf16 for the tensor-core products; accumulation is float32 either way.
+ * GRPO_E4M3 problems take FP8 operands with row scales and are run by
+ * grpo_loss_fwd_e4m3 / grpo_loss_bwd_e4m3 (their dH is bf16). */
+typedef enum grpo_dtype { GRPO_F32 = 0, GRPO_BF16 = 1, GRPO_E4M3 = 2 } grpo_dtype;
 
 typedef struct grpo_problem {
   int64_t N;            /* rows = num_seqs * seq_len */
-  int64_t d;            /* hidden size, multiple of 8 */
+  int64_t d;            /* hidden size, multiple of 8 (of 16 for GRPO_E4M3) */
   int64_t V;            /* vocab size */
   int32_t num_seqs;     /* B */
   int32_t seq_len;      /* T */
@@ -212,6 +214,65 @@ grpo_status grpo_loss_fwd_noalloc(const grpo_problem *problem, const void *H_pol
                                   const uint8_t *mask, const float *adv, float *logp_pol,
                                   float *logp_ref, float *lse_pol, float *loss, float *kl_mean,
                                   cudaStream_t stream);
+
+/*
+ * FP8 operands. The pages name Float8 training only as a feature that
+ * combines with the long-context loss (Unsloth "grpo-long-context" page, the
+ * hint listing the features that combine, item 3) and fix no format, so the
+ * format is OCP FP8 E4M3 (the "fn" flavour: no infinities, codes 0x7F and
+ * 0xFF are NaN, largest finite value 448) with one float32 scale per row:
+ * row r of an operand stands for s[r] * decode(q[r][:]). An e4m3 problem
+ * (problem->dtype = GRPO_E4M3) is the loss above evaluated on the
+ * dequantized H_pol, H_ref and W; dH and dW are its gradients with respect
+ * to the dequantized H_pol and W. The three products H W^T (reference and
+ * policy forward, backward recompute) run on e4m3 tensor-core operands with
+ * float32 accumulation, the row scales applied to the accumulator; the
+ * dH = dZ W and dW = dZ^T H products take bf16 roundings of the dequantized
+ * W and H_pol, since dZ keeps bf16.
+ *
+ * grpo_quantize_e4m3_rows turns float32 or bf16 rows into such operands, per
+ * row in float32 arithmetic: amax = max |x|, scale = amax / 448,
+ * q = e4m3(x * (448 / amax)) rounded to nearest even and saturated to
+ * +-448 (divisions and the product correctly rounded); a row of zeros gets
+ * scale 1 and zero codes.
+ *   x      device [rows, cols] of x_dtype (GRPO_F32 or GRPO_BF16), read only
+ *   q      device uint8 [rows, cols], written
+ *   scale  device float32 [rows], written
+ * INVALID_ARG for null pointers, rows < 0, cols < 1 or another x_dtype;
+ * UNSUPPORTED unless cols % 16 == 0 and x, q, scale are 16-byte aligned.
+ * rows = 0 launches nothing.
+ */
+grpo_status grpo_quantize_e4m3_rows(const void *x, grpo_dtype x_dtype, int64_t rows,
+                                    int64_t cols, uint8_t *q, float *scale,
+                                    cudaStream_t stream);
+
+/*
+ * grpo_loss_fwd for an e4m3 problem (problem->dtype = GRPO_E4M3, d % 16 == 0):
+ *   H_pol, H_ref  uint8 e4m3 [N, d] with s_pol, s_ref float32 [N]
+ *   W             uint8 e4m3 [V, d] with s_W float32 [V]
+ * every other argument and output as in grpo_loss_fwd (with ref_logp_given,
+ * H_ref and s_ref are not read and may be NULL). The workspace is sized by
+ * grpo_workspace_size on the same problem. grpo_loss_fwd and grpo_loss_bwd
+ * reject e4m3 problems (INVALID_ARG), and these two reject the others.
+ */
+grpo_status grpo_loss_fwd_e4m3(const grpo_problem *problem, const uint8_t *H_pol,
+                               const float *s_pol, const uint8_t *H_ref, const float *s_ref,
+                               const uint8_t *W, const float *s_W, const int32_t *ids,
+                               const uint8_t *mask, const float *adv, float *logp_pol,
+                               float *logp_ref, float *lse_pol, float *loss, float *kl_mean,
+                               void *workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * grpo_loss_bwd for an e4m3 problem: the operands as in grpo_loss_fwd_e4m3,
+ * dH bf16 [N, d] (the gradient with respect to the dequantized H_pol; rows
+ * of masked tokens are 0), dW float32 [V, d] or NULL as in grpo_loss_bwd.
+ */
+grpo_status grpo_loss_bwd_e4m3(const grpo_problem *problem, const uint8_t *H_pol,
+                               const float *s_pol, const uint8_t *W, const float *s_W,
+                               const int32_t *ids, const uint8_t *mask, const float *adv,
+                               const float *logp_pol, const float *logp_ref,
+                               const float *lse_pol, float grad_loss, void *dH, float *dW,
+                               void *workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /*
  * Synchronises `stream`, reads and clears the error word of a workspace
