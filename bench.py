@@ -289,6 +289,9 @@ def run_ours(args, w):
     inp = WL.make_inputs(w_r)
     n_valid = int(inp["mask"].sum())
     dt = torch.float32 if w.dtype == "f32" else torch.bfloat16
+    if args.fp8:
+        # e4m3 operands: the step quantizes H_pol, H_ref and W row-wise first
+        dt = torch.float8_e4m3fn
 
     eng = G.GRPOLoss(w.B, w.T, w.d, w.V, w.G, beta=w.beta, eps=w.eps,
                      std_unbiased=w.std_unbiased, dtype=dt, device=dev, compute_dW=args.dW,
@@ -298,7 +301,8 @@ def run_ours(args, w):
     d_in = {k: (v.to(dev) if v is not None else None) for k, v in inp.items()}
     rewards = d_in["rewards"]
     adv_in = d_in["adv"]
-    dH = torch.empty_like(d_in["H_pol"])
+    dH = (torch.empty(d_in["H_pol"].shape, dtype=torch.bfloat16, device=dev) if args.fp8
+          else torch.empty_like(d_in["H_pol"]))
     stream = torch.cuda.current_stream()
 
     if args.ref_given:
@@ -435,26 +439,39 @@ def run_ours(args, w):
         gemms = {k: prof[k] for k in ("fwd_gemm_lse", "bwd_dz_gemm", "bwd_dh_gemm",
                                       "bwd_dw_gemm") if prof[k][1]}
         peak = peaks["bf16_tflops_sustained"]
+        # e4m3 contractions: the measured bf16 peak times the nominal e4m3 / bf16
+        # dense ratio (4.5 / 2.25 PFLOP/s)
+        fp8_kernels = ("fwd_gemm_lse", "bwd_dz_gemm") if args.fp8 else ()
+
+        def kpeak(k):
+            return peak * 2.0 if k in fp8_kernels else peak
+
         roofline = None
         if gemms:  # (a replayed CUDA graph records no per-kernel events)
             dom = max(gemms, key=lambda k: gemms[k][0])
             dom_ms, dom_launches = gemms[dom]
             per_launch_flops = fl[dom] * args.steps / dom_launches
             achieved = per_launch_flops / (dom_ms / dom_launches / 1e3) / 1e12
-            roofline = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak,
-                        "unit": "TFLOP/s", "frac": achieved / peak,
-                        "traffic": measured_traffic(dom, w.name),
-                        "peak_kind": "bf16 sustained (%s)" % peaks["source"]}
+            roofline = {"bound": "tensor", "kernel": dom, "achieved": achieved,
+                        "peak": kpeak(dom), "unit": "TFLOP/s", "frac": achieved / kpeak(dom),
+                        "traffic": measured_traffic(dom, w.name + ("-e4m3" if args.fp8 else "")),
+                        "peak_kind": ("e4m3 = 2 x bf16 sustained (%s)" if dom in fp8_kernels
+                                      else "bf16 sustained (%s)") % peaks["source"]}
         launches = int(sum(v[1] for v in prof.values())) or graph_launches_per_step * args.steps
         kernels = {k: {"ms_per_step": v[0] / args.steps, "launches_per_step": v[1] / args.steps}
                    for k, v in prof.items() if v[1]}
         step_tflops = fl["step"] / (ms_step / 1e3) / 1e12
+        # time the step's GEMM flops would take at their own peaks
+        ideal_s = sum(fl[k] / (kpeak(k) * 1e12) for k in
+                      ("fwd_gemm_lse", "bwd_dz_gemm", "bwd_dh_gemm") +
+                      (("bwd_dw_gemm",) if args.dW else ()))
         cpu = cpu_oracle_sample(w, inp) if ws == 1 and not args.no_cpu_baseline else None
         line = {
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": "bf16" if w.dtype == "bf16" else "f32->bf16", "data": "synthetic",
+            "dtype": ("e4m3" if args.fp8 else "bf16" if w.dtype == "bf16" else "f32->bf16"),
+            "data": "synthetic",
             "config": {"workload": w.name, "prompts": w.prompts, "generations": w.G,
                        "completion_len": w.T, "tokens": w.N, "valid_tokens": n_valid,
                        "hidden": w.d, "vocab": w.V, "beta": w.beta, "dW": bool(args.dW),
@@ -462,14 +479,17 @@ def run_ours(args, w):
                                    "temperature": args.temperature,
                                    "ref_logp_given": bool(args.ref_given),
                                    "cluster_mode": args.cluster_mode,
-                                   "cuda_graph": bool(args.graph)},
+                                   "cuda_graph": bool(args.graph),
+                                   "operands": ("e4m3 row-scaled H W^T GEMMs (quantized from "
+                                                "bf16 inside the step); bf16 dH/dW GEMMs"
+                                                if args.fp8 else w.dtype)},
                        "flops_per_step": fl["step"],
                        "parallelism": "replicas" if ws > 1 else "single",
                        "l2": "inputs larger than L2 (H_pol+H_ref+W = %.2f GB)"
                              % ((inp["H_pol"].numel() * 2 + inp["W"].numel()) *
                                 inp["W"].element_size() / 1e9)},
             "tflops_per_step": step_tflops,
-            "frac_of_peak": step_tflops / peak,
+            "frac_of_peak": ideal_s / (ms_step / 1e3),
             "peak": {"bf16_tflops_sustained": peak, "source": peaks["source"]},
             "roofline": roofline,
             "kernels": kernels,
@@ -513,6 +533,8 @@ def main():
     ap.add_argument("--cluster-mode", type=int, default=0, choices=[0, 1, 2],
                     help="GEMM tiling: 0 one CTA per tile, 1 CTA pairs (cta_group::2), "
                          "2 two-CTA clusters multicasting B")
+    ap.add_argument("--fp8", action="store_true",
+                    help="e4m3 operands for the H W^T GEMMs (row-wise quantized in the step)")
     ap.add_argument("--ref-given", action="store_true",
                     help="reference log-probs supplied; skip the reference GEMM half")
     args = ap.parse_args()

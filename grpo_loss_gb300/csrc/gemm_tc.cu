@@ -222,7 +222,7 @@ __device__ __forceinline__ float xform_logit(const GemmArgs& g, float z, float* 
   return u * g.x_inv_temp;
 }
 
-template <int MODE, int KIND>
+template <int MODE, int KIND, bool F8>
 __global__ void __launch_bounds__(kThreads, 1)
     k_gemm(const __grid_constant__ CUtensorMap mapA0, const __grid_constant__ CUtensorMap mapA1,
            const __grid_constant__ CUtensorMap mapB, const __grid_constant__ CUtensorMap mapC,
@@ -293,8 +293,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   // MODE_DW reduces over the chunk's tokens: two 64-wide K blocks per block
   const int nk = MODE == MODE_DW ? 2 * max(0, min(g.chunk_nb, nb - g.chunk_b0)) : g.nk;
   // e4m3 operands (logit GEMMs only): 128 elements per 128-byte stage row
-  const bool f8 = (MODE == MODE_FWD || MODE == MODE_DZ) && g.fp8 != 0;
-  const int kel = f8 ? 2 * kBK : kBK;
+  constexpr bool f8 = F8 && (MODE == MODE_FWD || MODE == MODE_DZ);
+  constexpr int kel = f8 ? 2 * kBK : kBK;
   const int b_k0 = MODE == MODE_DW ? g.chunk_b0 * kBM : 0;  // B's K offset (H^T columns)
 
   if (warp == 0) {
@@ -370,6 +370,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0 && leader) {
       const uint32_t idesc = f8 ? idesc_e4m3_f32(PAIR ? 2 * kBM : kBM, static_cast<uint32_t>(g.bn))
                                 : idesc_bf16_f32(PAIR ? 2 * kBM : kBM, static_cast<uint32_t>(g.bn));
+      static_assert(!F8 || MODE == MODE_FWD || MODE == MODE_DZ, "e4m3 logit GEMMs only");
       int s = 0;
       uint32_t ph = 0;
       int ab = 0;
@@ -404,13 +405,13 @@ __global__ void __launch_bounds__(kThreads, 1)
               const uint64_t ad = sdesc_kmajor_sw128(a_addr + k * 32);
               const uint64_t bd = sdesc_kmajor_sw128(b_addr + k * 32);
               const uint32_t acc = (kb | k) != 0;
-              if (PAIR) {
-                if (f8)
+              if constexpr (PAIR) {
+                if constexpr (f8)
                   umma_e4m3_pair(d_tmem, ad, bd, idesc, acc);
                 else
                   umma_bf16_pair(d_tmem, ad, bd, idesc, acc);
               } else {
-                if (f8)
+                if constexpr (f8)
                   umma_e4m3(d_tmem, ad, bd, idesc, acc);
                 else
                   umma_bf16(d_tmem, ad, bd, idesc, acc);
@@ -475,7 +476,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       float c_n = 0.f, lse2 = 0.f;
       bool live = false;
       float rs = 1.f;  // e4m3: this row's scale
-      if (f8 && in_range) rs = (MODE == MODE_FWD && un.side) ? g.sa1[row] : g.sa0[row];
+      if constexpr (f8) {
+        if (in_range) rs = (MODE == MODE_FWD && un.side) ? g.sa1[row] : g.sa0[row];
+      }
       if (MODE == MODE_FWD) {
         y = in_range ? g.ids[row] : -1;
       } else if (MODE == MODE_DZ) {
@@ -507,7 +510,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int c = 0; c < kVocabTile / 32; ++c) {
             uint32_t r[32];
             tmem_ld32_wait(tbase + c * 32, r);
-            if (f8) apply_fp8_scales(r, rs, g.sb, col_t + c * 32, g.V);
+            if constexpr (f8) apply_fp8_scales(r, rs, g.sb, col_t + c * 32, g.V);
             if (g.xform) {  // uniform across the grid
               float fp;
 #pragma unroll
@@ -560,7 +563,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (col0 >= g.V) break;  // uniform across the warp
             uint32_t r[32];
             tmem_ld32_wait(tbase + c * 32, r);
-            if (f8) apply_fp8_scales(r, rs, g.sb, col0, g.V);
+            if constexpr (f8) apply_fp8_scales(r, rs, g.sb, col0, g.V);
             float o[32];
             if (!g.xform) {
 #pragma unroll
@@ -723,18 +726,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int MODE, int KIND>
+template <int MODE, int KIND, bool F8 = false>
 cudaError_t set_smem_limit() {
-  return cudaFuncSetAttribute(k_gemm<MODE, KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  return cudaFuncSetAttribute(k_gemm<MODE, KIND, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               Cfg<KIND>::kSmemBytes);
 }
 
-template <int MODE, int KIND>
+template <int MODE, int KIND, bool F8 = false>
 cudaError_t launch_mode(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b,
                         const CUtensorMap& c, const GemmArgs& args, int grid,
                         cudaStream_t stream) {
   if (KIND == KIND_SINGLE) {
-    k_gemm<MODE, KIND_SINGLE><<<grid, kThreads, Cfg<KIND_SINGLE>::kSmemBytes, stream>>>(
+    k_gemm<MODE, KIND_SINGLE, F8><<<grid, kThreads, Cfg<KIND_SINGLE>::kSmemBytes, stream>>>(
         a0, a1, b, c, args);
     return cudaGetLastError();
   }
@@ -750,7 +753,7 @@ cudaError_t launch_mode(const CUtensorMap& a0, const CUtensorMap& a1, const CUte
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, k_gemm<MODE, KIND>, a0, a1, b, c, args);
+  return cudaLaunchKernelEx(&cfg, k_gemm<MODE, KIND, F8>, a0, a1, b, c, args);
 }
 
 }  // namespace
@@ -762,6 +765,8 @@ cudaError_t configure_kind() {
   cudaError_t e;
   if ((e = set_smem_limit<MODE_FWD, KIND>()) != cudaSuccess) return e;
   if ((e = set_smem_limit<MODE_DZ, KIND>()) != cudaSuccess) return e;
+  if ((e = set_smem_limit<MODE_FWD, KIND, true>()) != cudaSuccess) return e;
+  if ((e = set_smem_limit<MODE_DZ, KIND, true>()) != cudaSuccess) return e;
   if ((e = set_smem_limit<MODE_DH, KIND>()) != cudaSuccess) return e;
   return set_smem_limit<MODE_DW, KIND>();
 }
@@ -788,7 +793,7 @@ int gemm_pair_clusters() {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, k_gemm<MODE_FWD, KIND_PAIR>, &cfg) != cudaSuccess)
+  if (cudaOccupancyMaxActiveClusters(&n, k_gemm<MODE_FWD, KIND_PAIR, false>, &cfg) != cudaSuccess)
     return 0;
   return n;
 }
@@ -797,8 +802,14 @@ template <int KIND>
 cudaError_t launch_kind(int mode, const CUtensorMap& a0, const CUtensorMap& a1,
                         const CUtensorMap& b, const CUtensorMap& c, const GemmArgs& args,
                         int grid, cudaStream_t stream) {
-  if (mode == MODE_FWD) return launch_mode<MODE_FWD, KIND>(a0, a1, b, c, args, grid, stream);
-  if (mode == MODE_DZ) return launch_mode<MODE_DZ, KIND>(a0, a1, b, c, args, grid, stream);
+  // e4m3 operands: separate instantiations, so the bf16 kernels carry no
+  // trace of the scale arithmetic
+  if (mode == MODE_FWD)
+    return args.fp8 ? launch_mode<MODE_FWD, KIND, true>(a0, a1, b, c, args, grid, stream)
+                    : launch_mode<MODE_FWD, KIND>(a0, a1, b, c, args, grid, stream);
+  if (mode == MODE_DZ)
+    return args.fp8 ? launch_mode<MODE_DZ, KIND, true>(a0, a1, b, c, args, grid, stream)
+                    : launch_mode<MODE_DZ, KIND>(a0, a1, b, c, args, grid, stream);
   if (mode == MODE_DH) return launch_mode<MODE_DH, KIND>(a0, a1, b, c, args, grid, stream);
   return launch_mode<MODE_DW, KIND>(a0, a1, b, c, args, grid, stream);
 }

@@ -254,3 +254,60 @@ def test_e4m3_problems_need_the_e4m3_entry_points():
     with pytest.raises(G.GrpoError) as e:
         G.workspace_size(G.make_problem(2, 8, 40, 64, 2, dtype=F8))
     assert e.value.status == 2
+
+
+# ------------------------------------------------------------- full size
+
+class _SampledRows:
+    """Dequantized rows of a large operand, held for a sample of rows only;
+    indexing with sampled row numbers returns them (the oracle's per-row
+    functions read only the rows they are asked for)."""
+
+    def __init__(self, rows, data):
+        self.pos = {int(r): i for i, r in enumerate(rows)}
+        self.data = data
+
+    def __getitem__(self, idx):
+        idx = np.asarray(idx).reshape(-1)
+        return self.data[[self.pos[int(i)] for i in idx]]
+
+
+@pytest.mark.slow
+def test_e4m3_full_size_llama_sampled_rows():
+    """The Llama-3.1-8B-shaped 20K x 8 head with e4m3 operands quantized on the
+    GPU, in the benchmark's launch configuration: sampled rows against the
+    oracle's own quantization, the GPU's codes of those rows against the
+    oracle's byte for byte, and the loss against its definition over the
+    per-token outputs."""
+    import grpo_loss_gb300 as G
+    w = WL.LLAMA31_8B_20K
+    inp = WL.make_inputs(w)
+    adv32 = torch.from_numpy(oracle_adv(w, inp)).float()
+    res = _engine_run(w, inp, adv32)
+    rows = WL.sample_rows(w, inp["mask"], count=64)
+    # codes of the sampled rows, quantized on the GPU, byte for byte
+    qg, sg = G.quantize_e4m3_rows(inp["H_pol"][torch.from_numpy(rows)].cuda())
+    qo, so = O.quantize_e4m3_rows(inp["H_pol"][torch.from_numpy(rows)])
+    assert np.array_equal(qg.cpu().numpy(), qo) and np.array_equal(sg.cpu().numpy(), so)
+    Hp = _SampledRows(rows, O.dequantize_rows(qo, so))
+    Hr = _SampledRows(rows, O.dequantize_rows(*O.quantize_e4m3_rows(inp["H_ref"][torch.from_numpy(rows)])))
+    Wf = np.empty((w.V, w.d))
+    for r0 in range(0, w.V, 8192):
+        Wf[r0:r0 + 8192] = O.dequantize_rows(*O.quantize_e4m3_rows(inp["W"][r0:r0 + 8192]))
+    q, lse = O.token_logprobs(Hp, Wf, inp["ids"], rows=rows)
+    p, _ = O.token_logprobs(Hr, Wf, inp["ids"], rows=rows)
+    assert rel_err(res["logp_pol"][rows], q) < TOL_REL
+    assert rel_err(res["logp_ref"][rows], p) < TOL_REL
+    assert rel_err(res["lse_pol"][rows], lse) < TOL_REL
+    g = O.backward(Hp, Hr, Wf, inp["ids"], inp["mask"], adv32.double(), w.B, w.T, w.beta,
+                   rows=rows)
+    assert rel_l2(res["dH"][rows], g["dH"]) < TOL_DH_L2
+    for i in range(rows.size):
+        assert rel_l2(res["dH"][rows[i]], g["dH"][i]) < 3 * TOL_DH_L2, int(rows[i])
+    wts, _ = O.sequence_weights(inp["mask"], w.B, w.T)
+    kl = O.kl_estimator(res["logp_pol"], res["logp_ref"])
+    A = np.repeat(adv32.double().numpy(), w.T)
+    m = inp["mask"].numpy() > 0
+    loss = float(np.sum(np.where(m, wts * (-A + w.beta * kl), 0.0)))
+    assert abs(res["loss"] - loss) <= 1e-5 * abs(loss) + 1e-9
+    torch.cuda.empty_cache()
