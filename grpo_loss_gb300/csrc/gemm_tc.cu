@@ -208,6 +208,28 @@ __device__ __forceinline__ void apply_fp8_scales(uint32_t (&r)[32], float rs,
   }
 }
 
+// e4m3 operands: per-column factors k[j] = rs2 * sb[col0 + j] (rs2 the A
+// row's scale, times log2(e) where the caller wants log2-domain logits), 0 at
+// or past V.
+__device__ __forceinline__ void fp8_col_factors(float (&k)[32], float rs2,
+                                                const float* __restrict__ sb, int64_t col0,
+                                                int64_t V) {
+  if (col0 + 32 <= V) {
+    const float4* s4 = reinterpret_cast<const float4*>(sb + col0);
+#pragma unroll
+    for (int v = 0; v < 8; ++v) {
+      const float4 sv = __ldg(s4 + v);
+      k[4 * v] = rs2 * sv.x;
+      k[4 * v + 1] = rs2 * sv.y;
+      k[4 * v + 2] = rs2 * sv.z;
+      k[4 * v + 3] = rs2 * sv.w;
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) k[j] = col0 + j < V ? rs2 * __ldg(sb + col0 + j) : 0.f;
+  }
+}
+
 // Optional logit transform z' = f(z): scale, then softcap, then temperature;
 // also returns f'(z) for the backward.
 __device__ __forceinline__ float xform_logit(const GemmArgs& g, float z, float* fprime) {
@@ -510,21 +532,34 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int c = 0; c < kVocabTile / 32; ++c) {
             uint32_t r[32];
             tmem_ld32_wait(tbase + c * 32, r);
-            if constexpr (f8) apply_fp8_scales(r, rs, g.sb, col_t + c * 32, g.V);
-            if (g.xform) {  // uniform across the grid
+            const int64_t col0 = col_t + c * 32;
+            // z: log2-domain logits; r keeps what the target gather reads
+            float z[32];
+            if (g.xform) {  // uniform across the grid: natural-unit logits first
+              if constexpr (f8) apply_fp8_scales(r, rs, g.sb, col0, g.V);
               float fp;
 #pragma unroll
-              for (int j = 0; j < 32; ++j)
+              for (int j = 0; j < 32; ++j) {
                 r[j] = __float_as_uint(xform_logit(g, __uint_as_float(r[j]), &fp));
+                z[j] = __uint_as_float(r[j]) * kLog2e;
+              }
+            } else if constexpr (f8) {
+              float k[32];  // one product per logit: acc * (rs log2(e) sb[col])
+              fp8_col_factors(k, rs * kLog2e, g.sb, col0, g.V);
+#pragma unroll
+              for (int j = 0; j < 32; ++j) z[j] = __uint_as_float(r[j]) * k[j];
+            } else {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) z[j] = __uint_as_float(r[j]) * kLog2e;
             }
-            const int64_t col0 = col_t + c * 32;
-            float z[32];
+            if (col0 + 32 > g.V) {  // the ragged last vocab tile only (uniform)
+#pragma unroll
+              for (int j = 0; j < 32; ++j)
+                if (col0 + j >= g.V) z[j] = -INFINITY;
+            }
             float cm = -INFINITY;
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              z[j] = (col0 + j < g.V) ? __uint_as_float(r[j]) * kLog2e : -INFINITY;
-              cm = fmaxf(cm, z[j]);
-            }
+            for (int j = 0; j < 32; ++j) cm = fmaxf(cm, z[j]);
             if (cm > m2) {
               const float sc = ex2_approx(m2 - cm);
               s_run *= sc;
@@ -546,6 +581,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
               for (int j = 0; j < 32; ++j)
                 if (j == off) zt = __uint_as_float(r[j]);
+              // e4m3 without transforms: r holds the raw accumulator (an id at
+              // or past V, flagged by the row plan, reads no scale)
+              if constexpr (f8) {
+                if (!g.xform) zt = y < g.V ? zt * rs * __ldg(g.sb + y) : 0.f;
+              }
               if (in_range) g.zy[static_cast<int64_t>(un.side) * g.N + row] = zt;
             }
           }
@@ -563,12 +603,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (col0 >= g.V) break;  // uniform across the warp
             uint32_t r[32];
             tmem_ld32_wait(tbase + c * 32, r);
-            if constexpr (f8) apply_fp8_scales(r, rs, g.sb, col0, g.V);
             float o[32];
             if (!g.xform) {
+              // 2^(z log2(e) - lse2) with z log2(e) = acc * k[j]
+              float k[32];
+              if constexpr (f8) {
+                fp8_col_factors(k, rs * kLog2e, g.sb, col0, g.V);
+              } else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) k[j] = kLog2e;
+              }
 #pragma unroll
               for (int j = 0; j < 32; ++j)
-                o[j] = live ? c_n * ex2_approx(fmaf(__uint_as_float(r[j]), kLog2e, -lse2)) : 0.f;
+                o[j] = live ? c_n * ex2_approx(fmaf(__uint_as_float(r[j]), k[j], -lse2)) : 0.f;
               const int64_t off = static_cast<int64_t>(y) - col0;
               if (off >= 0 && off < 32) {
 #pragma unroll
@@ -577,6 +624,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
             } else {
               // dZ = c (softmax(z') - onehot) f'(z) with z' = f(z)
+              if constexpr (f8) apply_fp8_scales(r, rs, g.sb, col0, g.V);
               const int64_t off = static_cast<int64_t>(y) - col0;
 #pragma unroll
               for (int j = 0; j < 32; ++j) {

@@ -311,3 +311,24 @@ def test_e4m3_full_size_llama_sampled_rows():
     loss = float(np.sum(np.where(m, wts * (-A + w.beta * kl), 0.0)))
     assert abs(res["loss"] - loss) <= 1e-5 * abs(loss) + 1e-9
     torch.cuda.empty_cache()
+
+
+def test_e4m3_bad_token_is_reported():
+    """A valid row whose id is V, on a vocab whose last tile is ragged (V =
+    3000), so the id falls inside the last chunk's column window: the device
+    reports GRPO_ERR_BAD_TOKEN and reads no scale past the end of s_W."""
+    import grpo_loss_gb300 as G
+    w = WL.SMALL["qwen2.5-small"]
+    assert w.V % 256 != 0 and (w.V % 256) % 32 != 0
+    inp = WL.make_inputs(w)
+    assert int(inp["mask"][3]) == 1
+    ids = inp["ids"].clone()
+    ids[3] = w.V
+    adv32 = torch.from_numpy(oracle_adv(w, inp)).float()
+    dev = torch.device("cuda")
+    eng = G.GRPOLoss(w.B, w.T, w.d, w.V, w.G, beta=w.beta, eps=w.eps,
+                     std_unbiased=w.std_unbiased, dtype=F8, device=dev)
+    eng.forward(inp["H_pol"].to(dev), inp["H_ref"].to(dev), inp["W"].to(dev), ids.to(dev),
+                inp["mask"].to(dev), adv32.to(dev))
+    torch.cuda.synchronize()
+    assert G.device_status(eng.ws_fwd) == 6
