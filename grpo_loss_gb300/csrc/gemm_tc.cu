@@ -51,8 +51,18 @@ namespace {
 
 constexpr int kMaxStages = 6;
 constexpr int kAStageBytes = kBM * kBK * 2;  // 16 KB
-constexpr int kThreads = 192;
-constexpr int kEpiThreads = 128;
+// Warps: 0 TMA producer, 1 MMA issuer, then the epilogue, 4 warps (one per
+// TMEM lane quadrant) or, for the forward with HALVES = 2, 8: two per
+// quadrant, each taking one half of the tile's columns, so two warps share
+// each SM sub-partition's issue slot and hide each other's latency. That pays
+// where a tile's MMAs are short (few K bytes per row) and the epilogue would
+// be the bottleneck.
+template <int HALVES>
+struct Warps {
+  static constexpr int kHalves = HALVES;
+  static constexpr int kEpiThreads = 128 * kHalves;
+  static constexpr int kThreads = 64 + kEpiThreads;
+};
 constexpr uint32_t kTmemCols = 512;
 constexpr int kAccStride = 256;  // TMEM columns per accumulator buffer
 // MODE_DZ output staging: per epilogue warp two 32 x 32 bf16 tiles for dZ
@@ -244,8 +254,8 @@ __device__ __forceinline__ float xform_logit(const GemmArgs& g, float z, float* 
   return u * g.x_inv_temp;
 }
 
-template <int MODE, int KIND, bool F8>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int MODE, int KIND, bool F8, int HALVES>
+__global__ void __launch_bounds__(Warps<HALVES>::kThreads, 1)
     k_gemm(const __grid_constant__ CUtensorMap mapA0, const __grid_constant__ CUtensorMap mapA1,
            const __grid_constant__ CUtensorMap mapB, const __grid_constant__ CUtensorMap mapC,
            const GemmArgs g) {
@@ -279,7 +289,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int b = 0; b < 2; ++b) {
       mbar_init(&sh->acc_full[b], 1);
       // PAIR: both CTAs' epilogues arrive on the even CTA's barrier
-      mbar_init(&sh->acc_empty[b], PAIR ? 2 * kEpiThreads : kEpiThreads);
+      mbar_init(&sh->acc_empty[b],
+                PAIR ? 2 * Warps<HALVES>::kEpiThreads : Warps<HALVES>::kEpiThreads);
     }
     mbar_init(&sh->mma_done, 1);
     sh->abort = 0;
@@ -477,6 +488,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;  // TMEM lane quadrant this warp may access
     const int r_in_tile = q * 32 + lane;
+    // MODE_FWD: the half of each tile's columns this warp takes
+    static_assert(HALVES == 1 || MODE == MODE_FWD, "column halves in the forward only");
+    constexpr int kChunks = kVocabTile / 32 / HALVES;
+    const int half = (warp - 2) >> 2;
     const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
     // MODE_DZ: this warp's staging tiles (dZ 0-1, dZ^T 2-3) and the chunk
     // counter picking one of each pair
@@ -529,7 +544,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (MODE == MODE_FWD) {
           float ts = 0.f;  // this tile's sum, relative to m2
 #pragma unroll 1
-          for (int c = 0; c < kVocabTile / 32; ++c) {
+          for (int c = half * kChunks; c < (half + 1) * kChunks; ++c) {
             uint32_t r[32];
             tmem_ld32_wait(tbase + c * 32, r);
             const int64_t col0 = col_t + c * 32;
@@ -567,14 +582,20 @@ __global__ void __launch_bounds__(kThreads, 1)
               ts *= sc;
               m2 = cm;
             }
-            float e[32];
+            // A half whose columns so far all lie at or past V (a slice made of
+            // the ragged last tile alone) still has m2 = -inf: it adds nothing,
+            // and its partial stays (-inf, 0), which the finish kernel's merge
+            // weighs by 2^-inf = 0.
+            if (m2 != -INFINITY) {
+              float e[32];
 #pragma unroll
-            for (int j = 0; j < 32; ++j) e[j] = ex2_approx(z[j] - m2);
+              for (int j = 0; j < 32; ++j) e[j] = ex2_approx(z[j] - m2);
 #pragma unroll
-            for (int w = 16; w >= 1; w >>= 1)
+              for (int w = 16; w >= 1; w >>= 1)
 #pragma unroll
-              for (int j = 0; j < w; ++j) e[j] += e[j + w];
-            ts += e[0];
+                for (int j = 0; j < w; ++j) e[j] += e[j + w];
+              ts += e[0];
+            }
             const int64_t off = static_cast<int64_t>(y) - col0;
             if (off >= 0 && off < 32) {
               float zt = 0.f;
@@ -745,7 +766,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       if (MODE == MODE_FWD && un.valid) {
         const int64_t pidx =
-            (static_cast<int64_t>(un.side) * g.nblk_max + un.jj) * g.n_vs + un.vs;
+            ((static_cast<int64_t>(un.side) * g.nblk_max + un.jj) * g.n_vs + un.vs) *
+                HALVES + half;
         g.part[pidx * kBM + r_in_tile] = make_float2(m2, s_run);
       }
     }
@@ -774,24 +796,25 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int MODE, int KIND, bool F8 = false>
+template <int MODE, int KIND, bool F8 = false, int HALVES = 1>
 cudaError_t set_smem_limit() {
-  return cudaFuncSetAttribute(k_gemm<MODE, KIND, F8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              Cfg<KIND>::kSmemBytes);
+  return cudaFuncSetAttribute(k_gemm<MODE, KIND, F8, HALVES>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<KIND>::kSmemBytes);
 }
 
-template <int MODE, int KIND, bool F8 = false>
+template <int MODE, int KIND, bool F8 = false, int HALVES = 1>
 cudaError_t launch_mode(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b,
                         const CUtensorMap& c, const GemmArgs& args, int grid,
                         cudaStream_t stream) {
   if (KIND == KIND_SINGLE) {
-    k_gemm<MODE, KIND_SINGLE, F8><<<grid, kThreads, Cfg<KIND_SINGLE>::kSmemBytes, stream>>>(
+    k_gemm<MODE, KIND_SINGLE, F8, HALVES>
+        <<<grid, Warps<HALVES>::kThreads, Cfg<KIND_SINGLE>::kSmemBytes, stream>>>(
         a0, a1, b, c, args);
     return cudaGetLastError();
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.blockDim = dim3(Warps<HALVES>::kThreads, 1, 1);
   cfg.dynamicSmemBytes = Cfg<KIND>::kSmemBytes;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -801,7 +824,7 @@ cudaError_t launch_mode(const CUtensorMap& a0, const CUtensorMap& a1, const CUte
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, k_gemm<MODE, KIND, F8>, a0, a1, b, c, args);
+  return cudaLaunchKernelEx(&cfg, k_gemm<MODE, KIND, F8, HALVES>, a0, a1, b, c, args);
 }
 
 }  // namespace
@@ -814,6 +837,8 @@ cudaError_t configure_kind() {
   if ((e = set_smem_limit<MODE_FWD, KIND>()) != cudaSuccess) return e;
   if ((e = set_smem_limit<MODE_DZ, KIND>()) != cudaSuccess) return e;
   if ((e = set_smem_limit<MODE_FWD, KIND, true>()) != cudaSuccess) return e;
+  if ((e = set_smem_limit<MODE_FWD, KIND, false, 2>()) != cudaSuccess) return e;
+  if ((e = set_smem_limit<MODE_FWD, KIND, true, 2>()) != cudaSuccess) return e;
   if ((e = set_smem_limit<MODE_DZ, KIND, true>()) != cudaSuccess) return e;
   if ((e = set_smem_limit<MODE_DH, KIND>()) != cudaSuccess) return e;
   return set_smem_limit<MODE_DW, KIND>();
@@ -831,7 +856,7 @@ int gemm_pair_clusters() {
   // multicast kernels use the same resources); 0 if the device cannot run them
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2, 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.blockDim = dim3(Warps<2>::kThreads, 1, 1);
   cfg.dynamicSmemBytes = Cfg<KIND_PAIR>::kSmemBytes;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -841,7 +866,8 @@ int gemm_pair_clusters() {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, k_gemm<MODE_FWD, KIND_PAIR, false>, &cfg) != cudaSuccess)
+  if (cudaOccupancyMaxActiveClusters(&n, k_gemm<MODE_FWD, KIND_PAIR, false, 2>, &cfg) !=
+      cudaSuccess)
     return 0;
   return n;
 }
@@ -852,9 +878,13 @@ cudaError_t launch_kind(int mode, const CUtensorMap& a0, const CUtensorMap& a1,
                         int grid, cudaStream_t stream) {
   // e4m3 operands: separate instantiations, so the bf16 kernels carry no
   // trace of the scale arithmetic
-  if (mode == MODE_FWD)
+  if (mode == MODE_FWD) {
+    if (args.fwd_halves == 2)
+      return args.fp8 ? launch_mode<MODE_FWD, KIND, true, 2>(a0, a1, b, c, args, grid, stream)
+                      : launch_mode<MODE_FWD, KIND, false, 2>(a0, a1, b, c, args, grid, stream);
     return args.fp8 ? launch_mode<MODE_FWD, KIND, true>(a0, a1, b, c, args, grid, stream)
                     : launch_mode<MODE_FWD, KIND>(a0, a1, b, c, args, grid, stream);
+  }
   if (mode == MODE_DZ)
     return args.fp8 ? launch_mode<MODE_DZ, KIND, true>(a0, a1, b, c, args, grid, stream)
                     : launch_mode<MODE_DZ, KIND>(a0, a1, b, c, args, grid, stream);

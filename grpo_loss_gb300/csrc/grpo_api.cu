@@ -195,6 +195,7 @@ struct Plan {
   int n_vt;          // vocab tiles of 256
   int n_vs;          // forward vocab slices
   int nk_d;          // K blocks over d
+  int fwd_halves;    // forward epilogue warps per row quadrant (column halves)
   int nk_v;          // K blocks over V
   int bn_dh;         // dH and dW tile width (columns of d)
   int n_nt;          // dH and dW column tiles
@@ -289,6 +290,7 @@ grpo_status make_plan(const grpo_problem* p, Plan* pl) {
       }
   }
   P.nk_d = static_cast<int>(ceil_div(P.d, P.e4m3 ? 2 * kBK : kBK));  // 128-byte K blocks
+  P.fwd_halves = P.nk_d <= kFwdSplitMaxKBlocks ? 2 : 1;
   P.nk_v = static_cast<int>(ceil_div(P.V, kBK));
   P.ldv = (P.V + 7) / 8 * 8;
   // widest tile over d (a multiple of 64, <= 256: dW reads H in 64-column
@@ -328,7 +330,7 @@ grpo_status make_plan(const grpo_problem* p, Plan* pl) {
   P.f_blk = take(sizeof(int) * P.nblk_max);
   P.f_inv = take(sizeof(int) * P.nblk_max);
   P.f_zy = take(sizeof(float) * 2 * P.N);
-  P.f_part = take(sizeof(float2) * 2ull * P.nblk_max * P.n_vs * kBM);
+  P.f_part = take(sizeof(float2) * 2ull * P.nblk_max * P.n_vs * P.fwd_halves * kBM);
   P.f_partials = take(sizeof(double) * 3 * kFinishGrid);
   if (P.f32) {
     P.f_hp16 = take(2ull * P.N * P.d);
@@ -566,13 +568,15 @@ grpo_status loss_fwd_impl(const grpo_problem* problem, const void* H_pol, const 
   g.sa0 = s_pol;
   g.sa1 = s_ref;
   g.sb = s_W;
+  g.fwd_halves = P.fwd_halves;
   const int64_t units = static_cast<int64_t>(g.n_sides) *
                         (pair ? (P.nblk_max + 1) / 2 : P.nblk_max) * P.n_vs;
   const int grid = gemm_grid(pair, P.sms, pair_clusters, units);
   LAUNCH(K_FWD_GEMM, stream, launch_gemm(MODE_FWD, kind, mHp, mHr, mW, mW, g, grid, stream));
 
   LAUNCH(K_FWD_FINISH, stream,
-         launch_fwd_finish(inv, mask, cnt, adv, zy, part, P.nblk_max, P.n_vs, P.N, P.B, P.T,
+         launch_fwd_finish(inv, mask, cnt, adv, zy, part, P.nblk_max, P.n_vs * P.fwd_halves,
+                           P.N, P.B, P.T,
                            problem->token_level, ref_given ? 1 : 0, problem->kl_mode,
                            logp_pol, logp_ref,
                            lse_pol, partials, kFinishGrid, stream));

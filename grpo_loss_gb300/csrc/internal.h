@@ -15,6 +15,13 @@ enum : uint32_t { ERRBIT_TIMEOUT = 1u, ERRBIT_BAD_TOKEN = 2u };
 constexpr int kBM = 128;         // rows per output tile (one TMEM lane per row)
 constexpr int kBK = 64;          // bf16 K elements per 128-byte swizzled row
 constexpr int kVocabTile = 256;  // vocab columns per tile in the logit GEMMs
+// The forward epilogue may split each tile's columns between two warps per
+// row quadrant, each half keeping its own (max, sum-exp) partial per row: it
+// does when the operand rows hold at most this many 128-byte K blocks (short
+// MMAs per tile, so the epilogue would be the bottleneck). Measured on GB300:
+// 12 blocks (e4m3, d = 1536) ran 15% faster split; 23 and 24 blocks ran
+// 0.5-1.3% faster unsplit.
+constexpr int kFwdSplitMaxKBlocks = 16;
 
 // Element types of the operands a kernel reads.
 enum ElemType : int { ELT_BF16 = 0, ELT_F32 = 1, ELT_E4M3 = 2 };
@@ -38,7 +45,7 @@ struct GemmArgs {
   int64_t N, d, V;
   const int32_t* ids;
   float* zy;              // MODE_FWD: target logits [2][N]
-  float2* part;           // MODE_FWD: (max2, sumexp2) [2 * nblk_max][n_vs][128]
+  float2* part;           // MODE_FWD: (max2, sumexp2) [2 * nblk_max][n_vs * fwd_halves][128]
   const float* lse;       // MODE_DZ: policy logsumexp [N]
   const float* coef;      // MODE_DZ: c_n [N]
   __nv_bfloat16* dz;      // MODE_DZ: chunk of dZ, [chunk_nb * 128][ldz]
@@ -61,6 +68,7 @@ struct GemmArgs {
   const float* sa0;       // row scales of A (policy rows)
   const float* sa1;       // MODE_FWD: row scales of the reference rows
   const float* sb;        // row scales of B (the vocab rows of W)
+  int fwd_halves;         // MODE_FWD: 1 or 2 epilogue warps per row quadrant
 };
 
 // Profiling kinds (one per kernel the library launches).

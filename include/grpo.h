@@ -202,9 +202,10 @@ grpo_status grpo_loss_bwd(const grpo_problem *problem, const void *H_pol, const 
  * different host threads) race and must not be issued. Returns
  * GRPO_ERR_WORKSPACE when the problem needs more scratch than the array
  * holds (grpo_workspace_size gives the forward's need: for bf16 inputs
- * 8 + 16 * S bytes per token with S = 1..8 vocab slices, e.g. 72 bytes on
- * the Llama-8B head, so a few hundred thousand tokens fit; float32 inputs
- * also need bf16 copies of H_pol, H_ref and W).
+ * 8 + 16 * S * h bytes per token with S = 1..8 vocab slices and h = 2 when
+ * d <= 1024, else 1, e.g. 72 bytes on the Llama-8B head, so a few hundred
+ * thousand tokens fit; float32 inputs also need bf16 copies of H_pol, H_ref
+ * and W).
  * A device-detected error (a valid token id outside [0, V), an expired
  * pipeline wait) makes *loss NaN, since there is no workspace to query.
  */
