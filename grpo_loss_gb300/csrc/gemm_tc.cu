@@ -52,11 +52,12 @@ namespace {
 constexpr int kMaxStages = 6;
 constexpr int kAStageBytes = kBM * kBK * 2;  // 16 KB
 // Warps: 0 TMA producer, 1 MMA issuer, then the epilogue, 4 warps (one per
-// TMEM lane quadrant) or, for the forward with HALVES = 2, 8: two per
-// quadrant, each taking one half of the tile's columns, so two warps share
-// each SM sub-partition's issue slot and hide each other's latency. That pays
-// where a tile's MMAs are short (few K bytes per row) and the epilogue would
-// be the bottleneck.
+// TMEM lane quadrant) or, for the forward and the dZ recompute with
+// HALVES = 2, 8: two per quadrant, each taking one half of the tile's
+// columns, so two warps share each SM sub-partition's issue slot and hide
+// each other's latency. That pays where a tile's MMAs are short (few K bytes
+// per row) and the epilogue would be the bottleneck. A split dZ kernel stages
+// dZ only (two 2 KB tiles per warp in the same 32 KB), so it runs without dW.
 template <int HALVES>
 struct Warps {
   static constexpr int kHalves = HALVES;
@@ -488,14 +489,17 @@ __global__ void __launch_bounds__(Warps<HALVES>::kThreads, 1)
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;  // TMEM lane quadrant this warp may access
     const int r_in_tile = q * 32 + lane;
-    // MODE_FWD: the half of each tile's columns this warp takes
-    static_assert(HALVES == 1 || MODE == MODE_FWD, "column halves in the forward only");
+    // MODE_FWD, MODE_DZ: the half of each tile's columns this warp takes
+    static_assert(HALVES == 1 || MODE == MODE_FWD || MODE == MODE_DZ,
+                  "column halves in the logit GEMMs only");
     constexpr int kChunks = kVocabTile / 32 / HALVES;
     const int half = (warp - 2) >> 2;
     const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
     // MODE_DZ: this warp's staging tiles (dZ 0-1, dZ^T 2-3) and the chunk
     // counter picking one of each pair
-    uint8_t* my_out = smOut + (warp - 2) * 4 * kStageOutBytes;
+    // (split: two dZ tiles per warp, no dZ^T)
+    uint8_t* my_out = smOut + (warp - 2) * (HALVES == 2 ? 2 : 4) * kStageOutBytes;
+    const bool dzt = HALVES == 1 && g.dzt_on;
     uint32_t n_out = 0;
     int ab = 0;
     uint32_t aph = 0;
@@ -619,7 +623,7 @@ __global__ void __launch_bounds__(Warps<HALVES>::kThreads, 1)
           // dZ rows of this warp in the chunk buffer: jj*128 + 32q .. +31
           const int32_t out_y = un.jj * kBM + q * 32;
 #pragma unroll 1
-          for (int c = 0; c < kVocabTile / 32; ++c) {
+          for (int c = half * kChunks; c < (half + 1) * kChunks; ++c) {
             const int64_t col0 = col_t + c * 32;
             if (col0 >= g.V) break;  // uniform across the warp
             uint32_t r[32];
@@ -664,7 +668,7 @@ __global__ void __launch_bounds__(Warps<HALVES>::kThreads, 1)
             // v ^ ((r >> 1) & 3)), then one lane stores it with TMA; columns
             // at or past V are clipped by the tensor map.
             uint8_t* buf = my_out + (n_out & 1u) * kStageOutBytes;
-            uint8_t* tbuf = my_out + (2 + (n_out & 1u)) * kStageOutBytes;
+            uint8_t* tbuf = dzt ? my_out + (2 + (n_out & 1u)) * kStageOutBytes : buf;
             // the bulk group of two chunks ago (which read buf and tbuf) is done
             if (lane == 0) tma_store_wait_read_1();
             __syncwarp();
@@ -674,7 +678,7 @@ __global__ void __launch_bounds__(Warps<HALVES>::kThreads, 1)
               *reinterpret_cast<uint4*>(buf + lane * 64 + pv * 16) =
                   make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
             }
-            if (g.dzt_on) {
+            if (dzt) {
               // dZ^T tile: row j (vocab column) holds this warp's 32 tokens;
               // this lane's token sits at byte 2 * lane of the row, in 16-byte
               // piece (lane >> 3) ^ ((j >> 1) & 3) of the 64-byte swizzle
@@ -691,7 +695,7 @@ __global__ void __launch_bounds__(Warps<HALVES>::kThreads, 1)
             __syncwarp();
             if (lane == 0) {
               tma_store_2d(&mapA1, buf, static_cast<int32_t>(col0), out_y);
-              if (g.dzt_on) tma_store_2d(&mapC, tbuf, out_y, static_cast<int32_t>(col0));
+              if (dzt) tma_store_2d(&mapC, tbuf, out_y, static_cast<int32_t>(col0));
               tma_store_commit();
             }
             ++n_out;
@@ -839,6 +843,8 @@ cudaError_t configure_kind() {
   if ((e = set_smem_limit<MODE_FWD, KIND, true>()) != cudaSuccess) return e;
   if ((e = set_smem_limit<MODE_FWD, KIND, false, 2>()) != cudaSuccess) return e;
   if ((e = set_smem_limit<MODE_FWD, KIND, true, 2>()) != cudaSuccess) return e;
+  if ((e = set_smem_limit<MODE_DZ, KIND, false, 2>()) != cudaSuccess) return e;
+  if ((e = set_smem_limit<MODE_DZ, KIND, true, 2>()) != cudaSuccess) return e;
   if ((e = set_smem_limit<MODE_DZ, KIND, true>()) != cudaSuccess) return e;
   if ((e = set_smem_limit<MODE_DH, KIND>()) != cudaSuccess) return e;
   return set_smem_limit<MODE_DW, KIND>();
@@ -879,15 +885,19 @@ cudaError_t launch_kind(int mode, const CUtensorMap& a0, const CUtensorMap& a1,
   // e4m3 operands: separate instantiations, so the bf16 kernels carry no
   // trace of the scale arithmetic
   if (mode == MODE_FWD) {
-    if (args.fwd_halves == 2)
+    if (args.epi_halves == 2)
       return args.fp8 ? launch_mode<MODE_FWD, KIND, true, 2>(a0, a1, b, c, args, grid, stream)
                       : launch_mode<MODE_FWD, KIND, false, 2>(a0, a1, b, c, args, grid, stream);
     return args.fp8 ? launch_mode<MODE_FWD, KIND, true>(a0, a1, b, c, args, grid, stream)
                     : launch_mode<MODE_FWD, KIND>(a0, a1, b, c, args, grid, stream);
   }
-  if (mode == MODE_DZ)
+  if (mode == MODE_DZ) {
+    if (args.epi_halves == 2)
+      return args.fp8 ? launch_mode<MODE_DZ, KIND, true, 2>(a0, a1, b, c, args, grid, stream)
+                      : launch_mode<MODE_DZ, KIND, false, 2>(a0, a1, b, c, args, grid, stream);
     return args.fp8 ? launch_mode<MODE_DZ, KIND, true>(a0, a1, b, c, args, grid, stream)
                     : launch_mode<MODE_DZ, KIND>(a0, a1, b, c, args, grid, stream);
+  }
   if (mode == MODE_DH) return launch_mode<MODE_DH, KIND>(a0, a1, b, c, args, grid, stream);
   return launch_mode<MODE_DW, KIND>(a0, a1, b, c, args, grid, stream);
 }

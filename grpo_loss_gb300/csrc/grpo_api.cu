@@ -568,7 +568,7 @@ grpo_status loss_fwd_impl(const grpo_problem* problem, const void* H_pol, const 
   g.sa0 = s_pol;
   g.sa1 = s_ref;
   g.sb = s_W;
-  g.fwd_halves = P.fwd_halves;
+  g.epi_halves = P.fwd_halves;
   const int64_t units = static_cast<int64_t>(g.n_sides) *
                         (pair ? (P.nblk_max + 1) / 2 : P.nblk_max) * P.n_vs;
   const int grid = gemm_grid(pair, P.sms, pair_clusters, units);
@@ -734,6 +734,8 @@ grpo_status loss_bwd_impl(const grpo_problem* problem, const void* H_pol, const 
     gz.fp8 = P.e4m3 ? 1 : 0;
     gz.sa0 = s_pol;
     gz.sb = s_W;
+    // short tiles: two epilogue warps per row quadrant (no dZ^T staging)
+    gz.epi_halves = (!P.dw && P.nk_d <= kDzSplitMaxKBlocks) ? 2 : 1;
     LAUNCH(K_BWD_DZ_GEMM, stream, launch_gemm(MODE_DZ, kind, mHp, mDzStore, mW, mDzTStore, gz, grid_dz, stream));
     GemmArgs gh = g;
     gh.bn = P.bn_dh;

@@ -22,6 +22,10 @@ constexpr int kVocabTile = 256;  // vocab columns per tile in the logit GEMMs
 // 12 blocks (e4m3, d = 1536) ran 15% faster split; 23 and 24 blocks ran
 // 0.5-1.3% faster unsplit.
 constexpr int kFwdSplitMaxKBlocks = 16;
+// The same split for the dZ recompute (dW off only: the split kernel stages
+// no dZ^T). Measured: 12 blocks (e4m3, d = 1536) ran 31% faster split; 23
+// and 24 blocks ran 2% faster unsplit.
+constexpr int kDzSplitMaxKBlocks = 16;
 
 // Element types of the operands a kernel reads.
 enum ElemType : int { ELT_BF16 = 0, ELT_F32 = 1, ELT_E4M3 = 2 };
@@ -45,7 +49,7 @@ struct GemmArgs {
   int64_t N, d, V;
   const int32_t* ids;
   float* zy;              // MODE_FWD: target logits [2][N]
-  float2* part;           // MODE_FWD: (max2, sumexp2) [2 * nblk_max][n_vs * fwd_halves][128]
+  float2* part;           // MODE_FWD: (max2, sumexp2) [2 * nblk_max][n_vs * epi_halves][128]
   const float* lse;       // MODE_DZ: policy logsumexp [N]
   const float* coef;      // MODE_DZ: c_n [N]
   __nv_bfloat16* dz;      // MODE_DZ: chunk of dZ, [chunk_nb * 128][ldz]
@@ -68,7 +72,7 @@ struct GemmArgs {
   const float* sa0;       // row scales of A (policy rows)
   const float* sa1;       // MODE_FWD: row scales of the reference rows
   const float* sb;        // row scales of B (the vocab rows of W)
-  int fwd_halves;         // MODE_FWD: 1 or 2 epilogue warps per row quadrant
+  int epi_halves;         // MODE_FWD, MODE_DZ: 1 or 2 epilogue warps per row quadrant
 };
 
 // Profiling kinds (one per kernel the library launches).
