@@ -241,7 +241,8 @@ grpo_status grpo_loss_fwd_noalloc(const grpo_problem *problem, const void *H_pol
  *   scale  device float32 [rows], written
  * INVALID_ARG for null pointers, rows < 0, cols < 1 or another x_dtype;
  * UNSUPPORTED unless cols % 16 == 0 and x, q, scale are 16-byte aligned.
- * rows = 0 launches nothing.
+ * rows = 0 launches nothing. x must be finite: a row holding an infinity or
+ * a NaN gets unspecified codes and scale (no error is reported).
  */
 grpo_status grpo_quantize_e4m3_rows(const void *x, grpo_dtype x_dtype, int64_t rows,
                                     int64_t cols, uint8_t *q, float *scale,
@@ -252,7 +253,9 @@ grpo_status grpo_quantize_e4m3_rows(const void *x, grpo_dtype x_dtype, int64_t r
  *   H_pol, H_ref  uint8 e4m3 [N, d] with s_pol, s_ref float32 [N]
  *   W             uint8 e4m3 [V, d] with s_W float32 [V]
  * every other argument and output as in grpo_loss_fwd (with ref_logp_given,
- * H_ref and s_ref are not read and may be NULL). The workspace is sized by
+ * H_ref and s_ref are not read and may be NULL). The scales must be finite
+ * (they are used as given; the NaN codes 0x7F and 0xFF propagate as NaN).
+ * s_W must be 16-byte aligned (UNSUPPORTED otherwise). The workspace is sized by
  * grpo_workspace_size on the same problem. grpo_loss_fwd and grpo_loss_bwd
  * reject e4m3 problems (INVALID_ARG), and these two reject the others.
  */
