@@ -119,3 +119,44 @@ def test_problem_struct_layout_matches_the_header(tmp_path):
     assert int(out["size"]) == ctypes.sizeof(L.Problem)
     for f in fields:
         assert int(out[f]) == getattr(L.Problem, f).offset, f
+
+
+def test_e4m3_calls_reject_bad_arguments_on_host(lib):
+    """The e4m3 entry points and the quantizer check their arguments before
+    any CUDA call (no GPU needed)."""
+    import torch
+    f, b = ctypes.c_size_t(0), ctypes.c_size_t(0)
+    # e4m3 rows are d bytes: d must be a multiple of 16 (8 suffices for bf16)
+    p8 = L.make_problem(8, 64, 264, 1024, 4, dtype=torch.float8_e4m3fn)
+    assert p8.dtype == L.GRPO_E4M3
+    assert lib.grpo_workspace_size(ctypes.byref(p8), ctypes.byref(f), ctypes.byref(b)) == 2
+    fake = ctypes.c_void_p(256)                      # aligned, never dereferenced
+    # a bf16 problem through the e4m3 forward, an e4m3 problem through the bf16 calls
+    pb = _problem()
+    args = [ctypes.byref(pb)] + [fake] * 14 + [fake, 1 << 20, None]
+    assert lib.grpo_loss_fwd_e4m3(*args) == 1
+    p8ok = L.make_problem(8, 64, 256, 1024, 4, dtype=torch.float8_e4m3fn)
+    args = [ctypes.byref(p8ok)] + [fake] * 11 + [fake, 1 << 20, None]
+    assert lib.grpo_loss_fwd(*args) == 1
+    args = [ctypes.byref(p8ok)] + [fake] * 8 + [1.0, fake, None, fake, 1 << 20, None]
+    assert lib.grpo_loss_bwd(*args) == 1
+    # missing scales
+    args = [ctypes.byref(p8ok), fake, None, fake, fake, fake, fake] + [fake] * 8 + [fake, 1 << 20,
+                                                                               None]
+    assert lib.grpo_loss_fwd_e4m3(*args) == 1
+    args = [ctypes.byref(p8ok), fake, fake, fake, None] + [fake] * 6 + [1.0, fake, None, fake,
+                                                                     1 << 20, None]
+    assert lib.grpo_loss_bwd_e4m3(*args) == 1
+    # s_W must be 16-byte aligned (it is read with 16-byte loads)
+    odd = ctypes.c_void_p(260)
+    args = [ctypes.byref(p8ok), fake, fake, fake, fake, fake, odd] + [fake] * 8 + [fake, 1 << 20,
+                                                                              None]
+    assert lib.grpo_loss_fwd_e4m3(*args) == 2
+    # the quantizer
+    q = lib.grpo_quantize_e4m3_rows
+    assert q(None, L.GRPO_BF16, 4, 32, fake, fake, None) == 1
+    assert q(fake, L.GRPO_E4M3, 4, 32, fake, fake, None) == 1
+    assert q(fake, L.GRPO_BF16, -1, 32, fake, fake, None) == 1
+    assert q(fake, L.GRPO_BF16, 4, 0, fake, fake, None) == 1
+    assert q(fake, L.GRPO_BF16, 4, 24, fake, fake, None) == 2
+    assert q(odd, L.GRPO_F32, 4, 32, fake, fake, None) == 2

@@ -13,18 +13,21 @@ from grpo_loss_gb300 import workloads as WL
 pytestmark = pytest.mark.gpu
 
 
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float8_e4m3fn], ids=["bf16", "e4m3"])
 @pytest.mark.parametrize("w", [WL.SMALL["qwen2.5-small"], WL.SMALL["gpt-oss-small"]],
                          ids=lambda w: w.name)
-def test_step_replays_from_a_cuda_graph(w):
+def test_step_replays_from_a_cuda_graph(w, dtype):
+    """With e4m3 operands the captured step also holds the row quantization of
+    H_pol, H_ref and W."""
     import grpo_loss_gb300 as G
     dev = torch.device("cuda")
-    eng = G.GRPOLoss(w.B, w.T, w.d, w.V, w.G, beta=w.beta, eps=w.eps, dtype=torch.bfloat16,
+    eng = G.GRPOLoss(w.B, w.T, w.d, w.V, w.G, beta=w.beta, eps=w.eps, dtype=dtype,
                      chunk_rows=256, compute_dW=True)
     a = {k: v.to(dev) for k, v in WL.make_inputs(w).items() if v is not None}
     b = {k: v.to(dev) for k, v in WL.make_inputs(w.scaled(w.name, seed=w.seed + 9)).items()
          if v is not None}
     static = {k: v.clone() for k, v in a.items()}
-    dH = torch.empty_like(a["H_pol"])
+    dH = torch.empty(a["H_pol"].shape, dtype=torch.bfloat16, device=dev)
 
     def step(d):
         adv = eng.advantages(d["rewards"])
