@@ -23,11 +23,11 @@
 // dZ chunk (32 x 32 boxes, 64-byte swizzle) in MODE_DZ; mapC is the store map
 // of dZ^T in MODE_DZ when dW is requested.
 //
-// One CTA per SM, 6 warps: warp 0 issues TMA loads into a shared-memory
-// ring, warp 1 owns tensor memory and issues the MMAs, warps 2..5 run the
-// epilogue, each thread owning one accumulator row (one TMEM lane). Two
-// 256-column accumulators in tensor memory let the epilogue of one tile
-// overlap the MMAs of the next.
+// One CTA per SM, 6 warps (10 with the epilogue column split, below): warp 0
+// issues TMA loads into a shared-memory ring, warp 1 owns tensor memory and
+// issues the MMAs, warps 2..5 (2..9) run the epilogue, each thread owning
+// one accumulator row (one TMEM lane). Two 256-column accumulators in tensor
+// memory let the epilogue of one tile overlap the MMAs of the next.
 //
 // KIND selects the tiling: KIND_SINGLE, one CTA per 128-row tile; KIND_PAIR,
 // CTA pairs (clusters of 2) on tcgen05 cta_group::2: a pair
