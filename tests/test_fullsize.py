@@ -135,3 +135,53 @@ def test_wide_vocab_softcap_head():
     assert np.all(res["dH"].numpy()[rows][~m] == 0)
     del res
     torch.cuda.empty_cache()
+
+
+def _mem_available_gb() -> float:
+    try:
+        with open("/proc/meminfo") as fh:
+            for line in fh:
+                if line.startswith("MemAvailable:"):
+                    return int(line.split()[1]) / 1e6
+    except OSError:
+        pass
+    return 0.0
+
+
+def test_operands_past_2_31_elements_sampled_rows():
+    """524288 tokens on the Llama-8B head: H holds 2^31 elements (8.6 GB of
+    bf16 bytes), so any 32-bit element or byte offset would wrap. Sampled
+    rows, including the last valid row of the last sequence, against the
+    oracle; the loss against its definition over the per-token outputs."""
+    if _mem_available_gb() < 96:
+        pytest.skip("needs about 30 GB of host memory for the inputs")
+    w = WL.LLAMA31_8B_20K.scaled("llama3.1-head-512k", prompts=8, G=8, T=8192,
+                                 mask="pad_uniform", pad_lo=6144, pad_hi=8192, seed=1020)
+    assert w.N * w.d == 1 << 31
+    inp = WL.make_inputs(w)
+    adv32 = torch.from_numpy(oracle_adv(w, inp)).float()
+    res = gpu_run(w, inp, adv32)
+    rows = WL.sample_rows(w, inp["mask"], count=48)
+    m = inp["mask"].numpy()
+    last_valid = int(np.nonzero(m)[0][-1])
+    rows = np.unique(np.concatenate([rows, [last_valid]]))
+    valid = m[rows] > 0
+    Wf = O.to_f64(inp["W"])
+    q, lse = O.token_logprobs(inp["H_pol"], Wf, inp["ids"], rows=rows[valid])
+    p, _ = O.token_logprobs(inp["H_ref"], Wf, inp["ids"], rows=rows[valid])
+    assert rel_err(res["logp_pol"].numpy()[rows[valid]], q) < TOL_REL
+    assert rel_err(res["logp_ref"].numpy()[rows[valid]], p) < TOL_REL
+    assert rel_err(res["lse_pol"].numpy()[rows[valid]], lse) < TOL_REL
+    g = O.backward(inp["H_pol"], inp["H_ref"], Wf, inp["ids"], inp["mask"], adv32.double(),
+                   w.B, w.T, w.beta, rows=rows)
+    dH = res["dH"].numpy()[rows]
+    assert rel_l2(dH[valid], g["dH"][valid]) < TOL_DH_L2
+    assert np.all(dH[~valid] == 0)
+    wts, _ = O.sequence_weights(inp["mask"], w.B, w.T)
+    kl = O.kl_estimator(res["logp_pol"].numpy(), res["logp_ref"].numpy())
+    A = np.repeat(adv32.double().numpy(), w.T)
+    mm = m > 0
+    loss = float(np.sum(np.where(mm, wts * (-A + w.beta * kl), 0.0)))
+    assert abs(res["loss"] - loss) <= 1e-5 * abs(loss) + 1e-9
+    del res
+    torch.cuda.empty_cache()
