@@ -518,6 +518,10 @@ def run_ours(args, w):
                              % ((inp["H_pol"].numel() * 2 + inp["W"].numel()) *
                                 inp["W"].element_size() / 1e9)},
             "tflops_per_step": step_tflops,
+            # the same step without the backward's recompute GEMM in the count
+            # (forward GEMMs, dH and dW only): what an implementation keeping
+            # the logits would have to compute
+            "model_tflops_per_step": (fl["step"] - fl["bwd_dz_gemm"]) / (ms_step / 1e3) / 1e12,
             "frac_of_peak": ideal_s / (ms_step / 1e3),
             "peak": {"bf16_tflops_sustained": peak, "source": peaks["source"]},
             "roofline": roofline,
