@@ -522,6 +522,8 @@ def run_ours(args, w):
             # (forward GEMMs, dH and dW only): what an implementation keeping
             # the logits would have to compute
             "model_tflops_per_step": (fl["step"] - fl["bwd_dz_gemm"]) / (ms_step / 1e3) / 1e12,
+            # every row, padding included (value counts valid tokens only)
+            "all_rows_per_s": ws * w.N / (ms_step / 1e3),
             "frac_of_peak": ideal_s / (ms_step / 1e3),
             "peak": {"bf16_tflops_sustained": peak, "source": peaks["source"]},
             "roofline": roofline,

@@ -34,7 +34,7 @@ def case(request):
 
 def test_sampled_rows_match_oracle(case):
     w, inp, adv32, res = case
-    rows = WL.sample_rows(w, inp["mask"], count=96)
+    rows = WL.sample_rows(w, inp["mask"], count=2048)
     m = inp["mask"].numpy()[rows] > 0
     vrows = rows[m]
     Wf = O.to_f64(inp["W"])
@@ -183,5 +183,23 @@ def test_operands_past_2_31_elements_sampled_rows():
     mm = m > 0
     loss = float(np.sum(np.where(mm, wts * (-A + w.beta * kl), 0.0)))
     assert abs(res["loss"] - loss) <= 1e-5 * abs(loss) + 1e-9
+    del res
+    torch.cuda.empty_cache()
+
+
+def test_dW_full_size_qwen_head():
+    """dW (the lm_head gradient) at the full Qwen2.5-1.5B-shaped head
+    (16384 tokens, 12351 valid; d = 1536, V = 151936), in the benchmark's
+    default chunk plan, against the oracle's full float64 dW; dH on every row."""
+    w = WL.QWEN25_1P5B
+    inp = WL.make_inputs(w)
+    adv32 = torch.from_numpy(oracle_adv(w, inp)).float()
+    res = gpu_run(w, inp, adv32, want_dW=True)
+    g = O.backward(inp["H_pol"], inp["H_ref"], inp["W"], inp["ids"], inp["mask"], adv32.double(),
+                   w.B, w.T, w.beta, want_dW=True)
+    assert rel_l2(res["dW"].numpy(), g["dW"]) < TOL_DH_L2
+    assert rel_l2(res["dH"].numpy(), g["dH"]) < TOL_DH_L2
+    m = inp["mask"].numpy() > 0
+    assert np.all(res["dH"].numpy()[~m] == 0)
     del res
     torch.cuda.empty_cache()
