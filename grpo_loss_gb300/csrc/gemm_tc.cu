@@ -1,4 +1,13 @@
-// Persistent tcgen05 GEMM with three fused epilogues:
+// Persistent tcgen05 GEMM with three fused epilogues. The method: a
+// linear-cross-entropy style fused loss that never materialises the logits
+// (zjt100.com translation of the Unsloth GRPO blog, "Unsloth 高效 GRPO 算法";
+// aibit.im GRPO blog, memory-efficient linear kernels), with the logits kept
+// in float32 and the log-softmax taken with the logsumexp trick (Unsloth
+// "grpo-long-context" page, flattened sequence chunking; zjt100.com page, end
+// of "GRPO 的数学和发现的问题"), the backward recomputing them chunk by chunk
+// (Unsloth "grpo-long-context" page, offloaded log-softmax section), and the
+// optional logit scale, softcap and temperature of the chunked selective
+// log-softmax's arguments (same page, flattened sequence chunking).
 //
 //   MODE_FWD  Z = H W^T for policy and reference rows. Per row, an online
 //             max / sum-exp over the vocab tiles of one vocab slice (log2

@@ -1,5 +1,10 @@
 // Host side of the C ABI: argument checks, the workspace plan, the chunk
 // scheduler over the flattened token axis, TMA descriptors and launches.
+// The chunking follows the Unsloth "grpo-long-context" page, flattened
+// sequence chunking (Equations 1-3: the (batch x context) axis is cut into
+// chunks so only one chunk's logits exist at a time). There, a multiplier
+// sets the number of chunks; here a byte budget for the bf16 dZ chunk sets
+// their size.
 #include <math.h>
 #include <string.h>
 

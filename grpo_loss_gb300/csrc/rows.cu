@@ -25,6 +25,11 @@ __device__ __forceinline__ int warp_sum_i(int v) {
 }
 
 // ------------------------------------------------------------- advantages
+// Group-relative advantages: several answers per prompt are scored and the
+// advantage comes from the rewards statistically (aibit.im GRPO blog, GRPO
+// section; zjt100.com translation of the Unsloth GRPO blog, "GRPO 的数学和
+// 发现的问题": A is the advantage after all reward functions). The pages
+// print no formula; the reading is A = (r - mean_g) / (std_g + eps).
 // One warp per group of G contiguous rewards; mean and std in float64.
 __global__ void k_advantages(const float* __restrict__ r, int B, int G, float eps, int unbiased,
                              float* __restrict__ adv) {
@@ -67,6 +72,9 @@ __global__ void k_convert_bf16(const float* __restrict__ src, __nv_bfloat16* __r
 }
 
 // ------------------------------------------------------------- seq count
+// The loss scores completion tokens (Unsloth "grpo-long-context" page,
+// flattened sequence chunking: hidden states and completion ids are passed
+// together); masked positions are excluded.
 // One CTA per sequence: cnt_b = number of valid tokens; valid tokens whose id
 // is outside [0, V) raise the bad-token bit.
 __global__ void k_seq_count(const uint8_t* __restrict__ mask, const int32_t* __restrict__ ids,
@@ -157,6 +165,11 @@ __global__ void __launch_bounds__(1024) k_block_plan(const uint8_t* __restrict__
 }
 
 // ------------------------------------------------------------ fwd finish
+// The objective of the zjt100.com page, "GRPO 的数学和发现的问题": reverse KL
+// with Q the trained model and P the frozen reference, beta = 0.04, the
+// estimator exp(x) - x - 1 (x = p - q) with no extra Q factor, and the
+// exp(q - q.detach()) * A term, whose value is 1. The kl_mode variants read
+// the page's four experiments (same section).
 // Merge the vocab-slice partials into each row's logsumexp, form q, p, the
 // KL estimator and the weighted loss terms. Per-CTA float64 partial sums
 // (sum w*A, sum w*KL, sum m*KL) go to `partials` for a fixed-order final sum.
@@ -274,6 +287,9 @@ __global__ void k_fwd_reduce(const double* __restrict__ partials, int nparts,
 }
 
 // -------------------------------------------------------- bwd coefficient
+// The derivative of the per-token loss with respect to q (same page and
+// section): the detached factor passes A * dq, and d/dq of the estimator is
+// 1 - exp(x). So c_n = -dloss/dq_n, and dZ_n = c_n (softmax(z_n) - onehot).
 // c_n = g * w_n * (A_b + beta * (exp(p - q) - 1)) at valid rows, 0 elsewhere.
 // Token level: w_n = 1 / max(sum_b cnt_b, 1), the total formed per CTA.
 __global__ void k_bwd_coef(const uint8_t* __restrict__ mask, const int* __restrict__ cnt,
