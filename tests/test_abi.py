@@ -160,3 +160,43 @@ def test_e4m3_calls_reject_bad_arguments_on_host(lib):
     assert q(fake, L.GRPO_BF16, 4, 0, fake, fake, None) == 1
     assert q(fake, L.GRPO_BF16, 4, 24, fake, fake, None) == 2
     assert q(odd, L.GRPO_F32, 4, 32, fake, fake, None) == 2
+
+
+def test_plain_c_host_links_and_calls_the_library(tmp_path):
+    """A C program with no Python and no CUDA runtime calls links
+    libgrpo_gb300.so through include/grpo.h alone and gets host-side statuses
+    back (no GPU needed: every call below is rejected before any launch)."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no host C compiler")
+    if not os.path.exists(L.LIB_PATH):
+        pytest.skip("library not built (python -m grpo_loss_gb300.build)")
+    src = r'''
+#include <stdio.h>
+#include "grpo.h"
+int main(void) {
+  grpo_problem p = {0};
+  p.num_seqs = 8; p.seq_len = 64; p.N = 8 * 64; p.d = 256; p.V = 1024; p.group_size = 3;
+  p.beta = 0.04f; p.eps = 1e-4f; p.std_unbiased = 1; p.dtype = GRPO_BF16;
+  size_t f = 0, b = 0;
+  printf("%d\n", (int)grpo_workspace_size(&p, &f, &b));          /* group does not divide */
+  p.group_size = 4; p.dtype = GRPO_E4M3; p.d = 264;
+  printf("%d\n", (int)grpo_workspace_size(&p, &f, &b));          /* e4m3 needs d % 16 */
+  printf("%d\n", (int)grpo_advantages(NULL, 8, 4, 1e-4f, 1, NULL, NULL));
+  printf("%d\n", (int)grpo_quantize_e4m3_rows(NULL, GRPO_BF16, 4, 32, NULL, NULL, NULL));
+  printf("%s\n", grpo_status_string(GRPO_ERR_UNSUPPORTED));
+  return 0;
+}
+'''
+    c = tmp_path / "host.c"
+    c.write_text(src)
+    exe = tmp_path / "host"
+    libdir = os.path.dirname(L.LIB_PATH)
+    subprocess.run([cc, "-std=c11", "-Wall", "-I" + os.path.join(ROOT, "include"), str(c),
+                    "-L" + libdir, "-l:libgrpo_gb300.so", "-Wl,-rpath," + libdir, "-o", str(exe)],
+                   check=True)
+    out = subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split("\n")
+    assert out[:4] == ["1", "2", "1", "1"]
+    assert out[4] == "unsupported problem layout"
