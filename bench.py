@@ -565,9 +565,8 @@ def main():
     ap.add_argument("--temperature", type=float, default=0.0, help="logit temperature (0 = off)")
     ap.add_argument("--graph", action="store_true",
                     help="time the step replayed from a CUDA graph")
-    ap.add_argument("--cluster-mode", type=int, default=0, choices=[0, 1, 2],
-                    help="GEMM tiling: 0 one CTA per tile, 1 CTA pairs (cta_group::2), "
-                         "2 two-CTA clusters multicasting B")
+    ap.add_argument("--cluster-mode", type=int, default=0, choices=[0, 1],
+                    help="GEMM tiling: 0 one CTA per tile, 1 CTA pairs (cta_group::2)")
     ap.add_argument("--fp8", action="store_true",
                     help="e4m3 operands for the H W^T GEMMs (row-wise quantized in the step)")
     ap.add_argument("--ref-given", action="store_true",

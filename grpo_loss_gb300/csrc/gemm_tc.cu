@@ -46,11 +46,8 @@
 // issues the MMAs and multicasts its commits to both CTAs; both CTAs'
 // epilogue threads arrive on the even CTA's accumulator-empty barrier. The
 // pair takes blocks 2p and 2p + 1; a missing partner block loads rows past
-// the end of its tensor (zeros) and writes nothing. KIND_MCAST keeps one CTA
-// per 128-row tile but clusters two CTAs whose tiles share B: each loads half
-// of the B tile and multicasts it into both CTAs' shared memory (a third less
-// L2 traffic), and each MMA warp multicasts its stage-consumed commit so a
-// stage is refilled only after both CTAs are done with it.
+// the end of its tensor (zeros) and writes nothing. Every TMA load lands in
+// the issuing CTA's own shared memory (no multicast loads).
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -81,7 +78,7 @@ constexpr int kStageOutBytes = 32 * 64;
 constexpr int kOutBytes = 4 * 4 * kStageOutBytes;  // 32 KB
 constexpr float kLog2e = 1.4426950408889634f;
 
-enum : int { KIND_SINGLE = 0, KIND_PAIR = 1, KIND_MCAST = 2 };
+enum : int { KIND_SINGLE = 0, KIND_PAIR = 1 };
 
 template <int KIND>
 struct Cfg {
@@ -273,7 +270,6 @@ __global__ void __launch_bounds__(Warps<HALVES>::kThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   constexpr bool PAIR = KIND == KIND_PAIR;
-  constexpr bool MCAST = KIND == KIND_MCAST;
   constexpr bool CLUSTER = KIND != KIND_SINGLE;  // units are block pairs
   constexpr int kStages = Cfg<KIND>::kStages;
   constexpr int kBStageBytes = Cfg<KIND>::kBStageBytes;
@@ -293,8 +289,7 @@ __global__ void __launch_bounds__(Warps<HALVES>::kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&sh->full[s], 1);
-      // MCAST: both CTAs' MMA warps release a stage (its B half came from each)
-      mbar_init(&sh->empty[s], MCAST ? 2 : 1);
+      mbar_init(&sh->empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&sh->acc_full[b], 1);
@@ -328,11 +323,8 @@ __global__ void __launch_bounds__(Warps<HALVES>::kThreads, 1)
   const int n_units = unit_count<MODE, CLUSTER>(g, nb);
   const int b_rows = CLUSTER ? g.bn >> 1 : g.bn;  // B rows this CTA loads per stage
   const uint32_t b_bytes = static_cast<uint32_t>(b_rows) * kBK * 2;
-  // bytes the stage's full barrier waits for: both CTAs' loads for PAIR; own
-  // A plus both multicast B halves for MCAST
-  const uint32_t tx_bytes = PAIR    ? 2u * (kAStageBytes + b_bytes)
-                            : MCAST ? kAStageBytes + 2u * b_bytes
-                                    : kAStageBytes + b_bytes;
+  // bytes the stage's full barrier waits for (both CTAs' loads for PAIR)
+  const uint32_t tx_bytes = PAIR ? 2u * (kAStageBytes + b_bytes) : kAStageBytes + b_bytes;
   // MODE_DW reduces over the chunk's tokens: two 64-wide K blocks per block
   const int nk = MODE == MODE_DW ? 2 * max(0, min(g.chunk_nb, nb - g.chunk_b0)) : g.nk;
   // e4m3 operands (logit GEMMs only): 128 elements per 128-byte stage row
@@ -378,11 +370,6 @@ __global__ void __launch_bounds__(Warps<HALVES>::kThreads, 1)
               const uint32_t bar = mapa_shared(smem_u32(&sh->full[s]), 0);
               tma_load_2d_pair(smA + s * kAStageBytes, mA, bar, kb * kel, un.a_row);
               tma_load_2d_pair(smB + s * kBStageBytes, &mapB, bar, b_k0 + kb * kel, b_row);
-            } else if (MCAST) {
-              // own A; this CTA's half of the shared B tile, into both CTAs
-              tma_load_2d(smA + s * kAStageBytes, mA, &sh->full[s], kb * kel, un.a_row);
-              tma_load_2d_mcast(smB + s * kBStageBytes + rank * b_bytes, &mapB, &sh->full[s],
-                                b_k0 + kb * kel, b_row, 0x3);
             } else {
               tma_load_2d(smA + s * kAStageBytes, mA, &sh->full[s], kb * kel, un.a_row);
               tma_load_2d(smB + s * kBStageBytes, &mapB, &sh->full[s], b_k0 + kb * kel, b_row);
@@ -462,8 +449,6 @@ __global__ void __launch_bounds__(Warps<HALVES>::kThreads, 1)
             }
             if (PAIR)
               umma_commit_pair(&sh->empty[s], 0x3);  // both CTAs' stage s is free
-            else if (MCAST)
-              umma_commit_mcast(&sh->empty[s], 0x3);  // this CTA is done with both halves
             else
               umma_commit(&sh->empty[s]);
             if (++s == kStages) {
@@ -862,13 +847,12 @@ cudaError_t configure_kind() {
 cudaError_t gemm_configure() {
   cudaError_t e;
   if ((e = configure_kind<KIND_SINGLE>()) != cudaSuccess) return e;
-  if ((e = configure_kind<KIND_PAIR>()) != cudaSuccess) return e;
-  return configure_kind<KIND_MCAST>();
+  return configure_kind<KIND_PAIR>();
 }
 
 int gemm_pair_clusters() {
-  // co-resident clusters of two CTAs for the clustered kernels (the pair and
-  // multicast kernels use the same resources); 0 if the device cannot run them
+  // co-resident clusters of two CTAs for the pair kernels; 0 if the device
+  // cannot run them
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2, 1, 1);
   cfg.blockDim = dim3(Warps<2>::kThreads, 1, 1);
@@ -915,7 +899,6 @@ cudaError_t launch_gemm(int mode, int kind, const CUtensorMap& a0, const CUtenso
                         const CUtensorMap& b, const CUtensorMap& c, const GemmArgs& args,
                         int grid, cudaStream_t stream) {
   if (kind == KIND_PAIR) return launch_kind<KIND_PAIR>(mode, a0, a1, b, c, args, grid, stream);
-  if (kind == KIND_MCAST) return launch_kind<KIND_MCAST>(mode, a0, a1, b, c, args, grid, stream);
   return launch_kind<KIND_SINGLE>(mode, a0, a1, b, c, args, grid, stream);
 }
 

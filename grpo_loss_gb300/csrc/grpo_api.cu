@@ -236,7 +236,10 @@ grpo_status validate_problem(const grpo_problem* p) {
   if (p->token_level != 0 && p->token_level != 1) return GRPO_ERR_INVALID_ARG;
   if (p->ref_logp_given != 0 && p->ref_logp_given != 1) return GRPO_ERR_INVALID_ARG;
   if (p->kl_mode < 0 || p->kl_mode > 3) return GRPO_ERR_INVALID_ARG;
-  if (p->cluster_mode < 0 || p->cluster_mode > 2) return GRPO_ERR_INVALID_ARG;
+  if (p->cluster_mode < 0) return GRPO_ERR_INVALID_ARG;
+  // 2 was a two-CTA tiling that multicast B tiles; it measured slower than
+  // mode 0 under the power cap and was removed
+  if (p->cluster_mode > 1) return GRPO_ERR_UNSUPPORTED;
   for (float v : {p->logit_multiply, p->logit_divide, p->softcap, p->temperature})
     if (!isfinite(v) || v < 0.f) return GRPO_ERR_INVALID_ARG;
   return GRPO_OK;

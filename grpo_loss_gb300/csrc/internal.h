@@ -99,9 +99,8 @@ enum KernelKind : int {
 size_t gemm_smem_bytes();
 cudaError_t gemm_configure();  // sets the dynamic shared memory limit once
 int gemm_pair_clusters();      // co-resident two-CTA clusters of the clustered kernels
-// kind: 0 one CTA per tile; 1 CTA pairs on cta_group::2; 2 two-CTA clusters
-// multicasting B halves. Kinds 1 and 2 take an even grid launched as clusters
-// of 2, and B maps with boxes of bn / 2 rows.
+// kind: 0 one CTA per tile; 1 CTA pairs on cta_group::2, launched as an even
+// grid of two-CTA clusters with B maps of bn / 2 rows per box.
 cudaError_t launch_gemm(int mode, int kind, const CUtensorMap& a0, const CUtensorMap& a1,
                         const CUtensorMap& b, const CUtensorMap& c, const GemmArgs& args,
                         int grid, cudaStream_t stream);

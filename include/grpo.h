@@ -102,11 +102,11 @@ typedef struct grpo_problem {
   int32_t cluster_mode; /* GEMM tiling, when the column tile is at least 128
                            wide: 0 one CTA per 128-row tile (default);
                            1 CTA pairs on tcgen05 cta_group::2 (256-row tiles,
-                           half of each B tile per CTA); 2 two-CTA clusters
-                           that each load half of the shared B tile and
-                           multicast it to both. On a power-capped GB300 step
-                           mode 1 settled ~16% lower in clock and ran ~8%
-                           slower than mode 0. */
+                           half of each B tile per CTA). On a power-capped
+                           GB300 step mode 1 settled ~16% lower in clock and
+                           ran ~8% slower than mode 0. Any other value:
+                           GRPO_ERR_UNSUPPORTED if positive, INVALID_ARG if
+                           negative. */
 } grpo_problem;
 
 /*

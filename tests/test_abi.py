@@ -66,6 +66,8 @@ def _problem(**kw):
     ("chunk_rows", -1, 1),
     ("compute_dW", 2, 1),
     ("dtype", 7, 1),
+    ("cluster_mode", -1, 1),
+    ("cluster_mode", 2, 2),      # the removed multicast tiling
 ])
 def test_workspace_size_rejects_bad_problems_on_host(lib, field, value, expected):
     p = _problem()

@@ -155,7 +155,6 @@ CASES = [
     ("tiny-f32-transforms-token", WL.TINY, dict(XF, token_level=True)),
     ("qwen3-kl-forward", WL.SMALL["qwen3-small"], {"kl_mode": 3}),
     ("llama-pairs", WL.SMALL["llama3.1-small"], dict(cluster_mode=1, want_dW=True)),
-    ("llama-multicast", WL.SMALL["llama3.1-small"], dict(cluster_mode=2, want_dW=True)),
 ]
 
 

@@ -86,8 +86,8 @@ def test_reference_equal_policy_full_size(case):
 
 
 @pytest.mark.parametrize("variant", [{"softcap": 30.0, "temperature": 0.7, "token_level": True},
-                                     {"kl_mode": 3}, {"cluster_mode": 1}, {"cluster_mode": 2}],
-                         ids=["softcap-temp-token", "forward-kl", "cta-pairs", "b-multicast"])
+                                     {"kl_mode": 3}, {"cluster_mode": 1}],
+                         ids=["softcap-temp-token", "forward-kl", "cta-pairs"])
 def test_variant_sampled_rows_full_size(variant):
     """A variant at the full Llama-shaped size: sampled rows against the oracle."""
     w = WL.LLAMA31_8B_20K

@@ -59,12 +59,6 @@ CASES = [
     ("pairs-tiny-all", WL.TINY, dict(XF, token_level=True, kl_mode=2, cluster_mode=1)),
     ("pairs-d2880", WL.GPTOSS_20B.scaled("gpt-oss-d2880", prompts=1, G=4, T=160, d=2880, V=2056,
                                          pad_lo=80, pad_hi=160), {"cluster_mode": 1}),
-    # two-CTA clusters multicasting the shared B halves
-    ("mcast-llama", WL.SMALL["llama3.1-small"], {"cluster_mode": 2}),
-    ("mcast-qwen3-odd-blocks", WL.SMALL["qwen3-small"], {"cluster_mode": 2}),
-    ("mcast-tiny-all", WL.TINY, dict(XF, token_level=True, kl_mode=3, cluster_mode=2)),
-    ("mcast-d2880", WL.GPTOSS_20B.scaled("gpt-oss-d2880", prompts=1, G=4, T=160, d=2880, V=2056,
-                                         pad_lo=80, pad_hi=160), {"cluster_mode": 2}),
 ]
 
 
