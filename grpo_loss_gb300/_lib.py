@@ -79,6 +79,9 @@ _VP = ctypes.c_void_p
 _SIGNATURES = {
     "grpo_workspace_size": (ctypes.c_int, [ctypes.POINTER(Problem), ctypes.POINTER(ctypes.c_size_t),
                                            ctypes.POINTER(ctypes.c_size_t)]),
+    "grpo_chunk_plan": (ctypes.c_int, [ctypes.POINTER(Problem), ctypes.POINTER(ctypes.c_int64),
+                                       ctypes.POINTER(ctypes.c_int32),
+                                       ctypes.POINTER(ctypes.c_size_t)]),
     "grpo_advantages": (ctypes.c_int, [_VP, ctypes.c_int32, ctypes.c_int32, ctypes.c_float,
                                        ctypes.c_int32, _VP, _VP]),
     "grpo_loss_fwd": (ctypes.c_int, [ctypes.POINTER(Problem)] + [_VP] * 11 +
@@ -154,6 +157,14 @@ def workspace_size(problem: Problem):
     _check(lib().grpo_workspace_size(ctypes.byref(problem), ctypes.byref(f), ctypes.byref(b)),
            "grpo_workspace_size")
     return f.value, b.value
+
+
+def chunk_plan(problem: Problem):
+    """(chunk_rows, n_chunks, dz_chunk_bytes) of the backward's chunk plan."""
+    r, n, b = ctypes.c_int64(0), ctypes.c_int32(0), ctypes.c_size_t(0)
+    _check(lib().grpo_chunk_plan(ctypes.byref(problem), ctypes.byref(r), ctypes.byref(n),
+                                 ctypes.byref(b)), "grpo_chunk_plan")
+    return r.value, n.value, b.value
 
 
 def advantages(rewards: torch.Tensor, group_size: int, eps: float, std_unbiased: int,

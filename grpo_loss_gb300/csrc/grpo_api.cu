@@ -21,7 +21,7 @@ using namespace grpo;
 namespace {
 
 constexpr size_t kAlign = 256;
-constexpr uint64_t kDefaultDzBudget = 4ull << 30;  // bytes of the bf16 dZ chunk
+constexpr uint64_t kDefaultDzBudget = GRPO_DEFAULT_DZ_BUDGET_BYTES;  // bytes of the bf16 dZ chunk
 constexpr int kFinishGrid = 608;                   // CTAs of the per-token finish kernel
 constexpr int kMaxSlices = 8;                      // vocab slices per block in the forward
 constexpr double kL2ABudget = 40e6;                // bytes of A blocks kept resident in L2
@@ -433,6 +433,17 @@ grpo_status grpo_workspace_size(const grpo_problem* problem, size_t* fwd_bytes,
   if (st != GRPO_OK) return st;
   if (fwd_bytes) *fwd_bytes = P.f_total;
   if (bwd_bytes) *bwd_bytes = P.b_total;
+  return GRPO_OK;
+}
+
+grpo_status grpo_chunk_plan(const grpo_problem* problem, int64_t* chunk_rows, int32_t* n_chunks,
+                            size_t* dz_chunk_bytes) {
+  Plan P;
+  const grpo_status st = make_plan(problem, &P);
+  if (st != GRPO_OK) return st;
+  if (chunk_rows) *chunk_rows = static_cast<int64_t>(P.chunk_nb) * kBM;
+  if (n_chunks) *n_chunks = P.n_chunks;
+  if (dz_chunk_bytes) *dz_chunk_bytes = 2ull * P.chunk_nb * kBM * P.ldv;
   return GRPO_OK;
 }
 

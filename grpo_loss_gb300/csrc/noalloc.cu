@@ -20,17 +20,27 @@ namespace {
 static __device__ __align__(256) unsigned char g_noalloc_scratch[GRPO_NOALLOC_SCRATCH_BYTES];
 
 std::mutex g_mu;
-void* g_scratch_dev[64] = {nullptr};  // device address of the array, per device
+// Device address of the array, per device ordinal, looked up once. It
+// belongs to the context that was current then: after cudaDeviceReset (or
+// any teardown of the primary context) the module is loaded again and the
+// array may live elsewhere, so the entry point must not be used across a
+// reset.
+void* g_scratch_dev[64] = {nullptr};
 
 // After the forward has run: if a device-side check failed (a valid token
-// with an id outside [0, V), or an expired pipeline wait), mark the loss NaN.
-// This caller has no workspace through which to read the error word.
-__global__ void k_mark_loss_on_error(const uint32_t* err, float* loss) {
-  if (threadIdx.x == 0 && *err != 0u) *loss = __int_as_float(0x7fc00000);
+// with an id outside [0, V), or an expired pipeline wait), mark the loss and
+// the KL mean NaN. This caller has no workspace through which to read the
+// error word.
+__global__ void k_mark_loss_on_error(const uint32_t* err, float* loss, float* kl_mean) {
+  if (threadIdx.x == 0 && *err != 0u) {
+    *loss = __int_as_float(0x7fc00000);
+    if (kl_mean) *kl_mean = __int_as_float(0x7fc00000);
+  }
 }
 
 // First call on a device: look up the array's device address with that
-// device current. Host code may not use the array's name as an address.
+// device current. Host code may not use the array's name as an address: in
+// host code it names a host-side stand-in, not device memory.
 grpo_status scratch_for_current_device(void** ptr) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return GRPO_ERR_CUDA;
@@ -65,6 +75,7 @@ extern "C" grpo_status grpo_loss_fwd_noalloc(const grpo_problem* problem, const 
   st = grpo_loss_fwd(problem, H_pol, H_ref, W, ids, mask, adv, logp_pol, logp_ref, lse_pol,
                      loss, kl_mean, scratch, GRPO_NOALLOC_SCRATCH_BYTES, stream);
   if (st != GRPO_OK) return st;
-  k_mark_loss_on_error<<<1, 32, 0, stream>>>(static_cast<const uint32_t*>(scratch), loss);
+  k_mark_loss_on_error<<<1, 32, 0, stream>>>(static_cast<const uint32_t*>(scratch), loss,
+                                              kl_mean);
   return cudaGetLastError() == cudaSuccess ? GRPO_OK : GRPO_ERR_CUDA;
 }

@@ -118,6 +118,28 @@ grpo_status grpo_workspace_size(const grpo_problem *problem, size_t *fwd_bytes,
                                 size_t *bwd_bytes);
 
 /*
+ * The backward's chunk plan over the flattened (sequences x tokens) axis
+ * (Unsloth "grpo-long-context" page, flattened sequence chunking, Equations
+ * 1-3: only one chunk's logits exist at a time). The pages set the number of
+ * chunks by a multiplier; here the size of the bf16 dZ chunk sets it. With
+ * chunk_rows = 0 the chunk is the largest number of 128-row blocks whose
+ * dZ (blocks * 128 rows * ldv columns * 2 bytes, ldv = V rounded up to a
+ * multiple of 8) fits GRPO_DEFAULT_DZ_BUDGET_BYTES, rounded down to a
+ * multiple of SMs / gcd(SMs, dH column tiles) blocks when that many fit, so
+ * each chunk's dH GEMM fills whole waves of the device's SMs; otherwise it
+ * is chunk_rows rounded up to a multiple of 128; never more than the
+ * problem's blocks.
+ *   chunk_rows      rows per chunk (a multiple of 128)
+ *   n_chunks        chunks the backward launches (ceil of blocks / chunk)
+ *   dz_chunk_bytes  bytes of the dZ chunk buffer in the backward workspace
+ * Any output pointer may be NULL. Host-only apart from reading the current
+ * device's SM count.
+ */
+#define GRPO_DEFAULT_DZ_BUDGET_BYTES ((size_t)4 << 30)
+grpo_status grpo_chunk_plan(const grpo_problem *problem, int64_t *chunk_rows, int32_t *n_chunks,
+                            size_t *dz_chunk_bytes);
+
+/*
  * Group-relative advantages (aibit.im GRPO blog, GRPO section: several
  * answers per prompt are scored and an advantage is derived from the rewards
  * statistically; zjt100.com page, "GRPO 的数学和发现的问题": A is the
@@ -194,20 +216,25 @@ grpo_status grpo_loss_bwd(const grpo_problem *problem, const void *H_pol, const 
  * Scratch lives in a static device array of GRPO_NOALLOC_SCRATCH_BYTES that
  * every GPU loading the library holds until the process exits. Its device
  * address is looked up on the first call on each device (with that device
- * current), so make that first call before any stream capture. The call
- * itself never allocates (no cudaMalloc or cudaFree).
+ * current), so make that first call before any stream capture. The address
+ * belongs to that device's context: do not use this entry point across a
+ * cudaDeviceReset or any other teardown of the context. The call itself
+ * never allocates (no cudaMalloc or cudaFree).
  *
  * Every call on a device shares the one array, and the array keeps the last
  * call's contents: calls that may overlap on the GPU (different streams, or
  * different host threads) race and must not be issued. Returns
- * GRPO_ERR_WORKSPACE when the problem needs more scratch than the array
- * holds (grpo_workspace_size gives the forward's need: for bf16 inputs
- * 8 + 16 * S * h bytes per token with S = 1..8 vocab slices and h = 2 when
- * d <= 1024, else 1, e.g. 72 bytes on the Llama-8B head, so a few hundred
- * thousand tokens fit; float32 inputs also need bf16 copies of H_pol, H_ref
- * and W).
+ * GRPO_ERR_WORKSPACE, before any launch, when the problem needs more scratch
+ * than the array holds. The need is grpo_workspace_size's forward bytes on
+ * the device the call runs on: query it there and compare it with
+ * GRPO_NOALLOC_SCRATCH_BYTES, since it depends on the device's SM count.
+ * For bf16 inputs it is about 8 + 16 * S * h bytes per token with S = 1..8
+ * vocab slices and h = 2 when d <= 1024, else 1 (e.g. 72 bytes on the
+ * Llama-8B head on a 152-SM GPU, so a few hundred thousand tokens fit);
+ * float32 inputs also need bf16 copies of H_pol, H_ref and W.
  * A device-detected error (a valid token id outside [0, V), an expired
- * pipeline wait) makes *loss NaN, since there is no workspace to query.
+ * pipeline wait) makes *loss and *kl_mean NaN, since there is no workspace
+ * to query; the per-token outputs are then undefined.
  */
 #define GRPO_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
 grpo_status grpo_loss_fwd_noalloc(const grpo_problem *problem, const void *H_pol,

@@ -70,3 +70,24 @@ def rel_l2(a, b) -> float:
     b = np.asarray(b, np.float64)
     nb = np.linalg.norm(b)
     return float(np.linalg.norm(a - b) / nb) if nb > 0 else float(np.linalg.norm(a))
+
+
+def x_and_kl_close(x_gpu, x_or, what: str = "") -> None:
+    """x = p - q and KL = exp(x) - x - 1 at sampled valid rows: each within
+    1e-3 relative of the oracle's, with absolute floors of 1e-3 of the
+    sample's rms x and of its mean KL. The floors keep rows with x near 0
+    (where a tiny KL's relative error means nothing) to the size of the
+    term the loss carries, beta * mean KL."""
+    from oracle import grpo_oracle as O
+    x_gpu = np.asarray(x_gpu, np.float64)
+    x_or = np.asarray(x_or, np.float64)
+    zero = np.zeros_like(x_or)
+    kl_gpu, kl_or = O.kl_estimator(zero, x_gpu), O.kl_estimator(zero, x_or)
+    ax = 1e-3 * np.sqrt(np.mean(x_or ** 2))
+    ak = 1e-3 * np.mean(kl_or)
+    dx = np.abs(x_gpu - x_or)
+    dk = np.abs(kl_gpu - kl_or)
+    assert np.all(dx <= TOL_REL * np.abs(x_or) + ax), \
+        "x %s: max |dx| %.3g, floor %.3g" % (what, dx.max(), ax)
+    assert np.all(dk <= TOL_REL * np.abs(kl_or) + ak), \
+        "KL %s: max |dKL| %.3g, floor %.3g" % (what, dk.max(), ak)

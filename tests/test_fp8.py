@@ -18,7 +18,7 @@ import torch
 
 from grpo_loss_gb300 import workloads as WL
 from oracle import grpo_oracle as O
-from tests.parity_util import TOL_DH_L2, TOL_REL, oracle_adv, rel_err, rel_l2
+from tests.parity_util import TOL_DH_L2, TOL_REL, oracle_adv, rel_err, rel_l2, x_and_kl_close
 
 pytestmark = pytest.mark.gpu
 
@@ -298,6 +298,7 @@ def test_e4m3_full_size_llama_sampled_rows():
     assert rel_err(res["logp_pol"][rows], q) < TOL_REL
     assert rel_err(res["logp_ref"][rows], p) < TOL_REL
     assert rel_err(res["lse_pol"][rows], lse) < TOL_REL
+    x_and_kl_close(res["logp_ref"][rows] - res["logp_pol"][rows], p - q, "e4m3")
     g = O.backward(Hp, Hr, Wf, inp["ids"], inp["mask"], adv32.double(), w.B, w.T, w.beta,
                    rows=rows)
     assert rel_l2(res["dH"][rows], g["dH"]) < TOL_DH_L2

@@ -1,24 +1,31 @@
 """Parity at the full sizes of the five workloads, in the launch
 configuration the benchmark times (default chunk plan).
 
-The oracle cannot form every logit of these problems in float64, so it
-checks a seeded, stratified sample of rows one by one (log-probs,
-logsumexp and the dH row, which depends on that row alone), and the rest is
-checked through properties that hold at any size: masked rows are exactly
-zero, the loss equals its definition evaluated in float64 from the
-per-token outputs, and with the reference equal to the policy the KL is
+The loss and the KL mean are compared with the float64 oracle's full
+forward pass over every token, computed once on the host and stored under
+tests/golden/ with a digest of the inputs it used. Per-token quantities are
+checked on a seeded, stratified sample of rows one by one (log-probs,
+logsumexp, x = p - q, the KL term and the dH row, which depends on that row
+alone), and the rest through properties that hold at any size: masked rows
+are exactly zero, the loss equals its definition evaluated in float64 from
+the per-token outputs, and with the reference equal to the policy the KL is
 exactly zero and the loss is -mean(A)."""
+import json
+import os
+
 import numpy as np
 import pytest
 import torch
 
 from grpo_loss_gb300 import workloads as WL
 from oracle import grpo_oracle as O
-from tests.parity_util import TOL_DH_L2, TOL_REL, gpu_run, oracle_adv, rel_err, rel_l2
+from tests.parity_util import (TOL_DH_L2, TOL_REL, gpu_run, oracle_adv, rel_err, rel_l2,
+                               x_and_kl_close)
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
 BIG = [WL.QWEN25_1P5B, WL.LLAMA31_8B_20K, WL.QWEN3_8B_110K, WL.GPTOSS_20B]
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
 
 
 @pytest.fixture(scope="module", params=BIG, ids=lambda w: w.name)
@@ -43,6 +50,8 @@ def test_sampled_rows_match_oracle(case):
     assert rel_err(res["logp_pol"].numpy()[vrows], q) < TOL_REL
     assert rel_err(res["logp_ref"].numpy()[vrows], p) < TOL_REL
     assert rel_err(res["lse_pol"].numpy()[vrows], lse) < TOL_REL
+    x_gpu = res["logp_ref"].numpy()[vrows] - res["logp_pol"].numpy()[vrows]
+    x_and_kl_close(x_gpu, p - q, w.name)
     g = O.backward(inp["H_pol"], inp["H_ref"], Wf, inp["ids"], inp["mask"], adv32.double(),
                    w.B, w.T, w.beta, rows=rows)
     dH = res["dH"].numpy()[rows]
@@ -51,6 +60,29 @@ def test_sampled_rows_match_oracle(case):
     for i in np.nonzero(m)[0]:
         assert rel_l2(dH[i], g["dH"][i]) < 3 * TOL_DH_L2, int(rows[i])
     assert np.all(dH[~m] == 0)
+
+
+def test_loss_and_kl_match_the_full_oracle_forward(case):
+    """loss and kl_mean within 1e-3 relative of the oracle's full float64
+    forward over every token (tests/golden/make_fullsize_golden.py), on the
+    same inputs: the stored digest must equal this run's."""
+    w, inp, adv32, res = case
+    with open(os.path.join(GOLDEN, "fullsize_%s.json" % w.name)) as fh:
+        rec = json.load(fh)
+    assert WL.input_digest(inp) == rec["input_digest"], \
+        "inputs differ from the ones the stored oracle values were computed on"
+    assert adv32.tolist() == rec["adv_float32"]
+    m = inp["mask"].numpy() > 0
+    assert int(m.sum()) == rec["n_valid"]
+    assert abs(res["loss"] - rec["loss"]) <= TOL_REL * abs(rec["loss"]), (res["loss"], rec["loss"])
+    assert abs(res["kl_mean"] - rec["kl_mean"]) <= TOL_REL * abs(rec["kl_mean"]), \
+        (res["kl_mean"], rec["kl_mean"])
+    # sums over every valid token: a per-token bias would show here
+    q = res["logp_pol"].numpy()[m].astype(np.float64)
+    p = res["logp_ref"].numpy()[m].astype(np.float64)
+    assert abs(q.sum() - rec["sum_logp_pol"]) <= 1e-5 * abs(rec["sum_logp_pol"])
+    assert abs(p.sum() - rec["sum_logp_ref"]) <= 1e-5 * abs(rec["sum_logp_ref"])
+    assert abs(np.sum((p - q) ** 2) - rec["sum_x_sq"]) <= TOL_REL * rec["sum_x_sq"]
 
 
 def test_masked_rows_are_zero_everywhere(case):
@@ -103,6 +135,8 @@ def test_variant_sampled_rows_full_size(variant):
     p, _ = O.token_logprobs(inp["H_ref"], Wf, inp["ids"], rows=rows, xform=xf)
     assert rel_err(res["logp_pol"].numpy()[rows], q) < TOL_REL
     assert rel_err(res["logp_ref"].numpy()[rows], p) < TOL_REL
+    x_and_kl_close(res["logp_ref"].numpy()[rows] - res["logp_pol"].numpy()[rows], p - q,
+                   str(variant))
     g = O.backward(inp["H_pol"], inp["H_ref"], Wf, inp["ids"], inp["mask"], adv32.double(),
                    w.B, w.T, w.beta, rows=rows, token_level=variant.get("token_level", False),
                    xform=xf, kl_mode=variant.get("kl_mode", 0))
@@ -190,7 +224,7 @@ def test_operands_past_2_31_elements_sampled_rows():
 
 def test_dW_full_size_qwen_head():
     """dW (the lm_head gradient) at the full Qwen2.5-1.5B-shaped head
-    (16384 tokens, 12351 valid; d = 1536, V = 151936), in the benchmark's
+    (16384 tokens, 11998 valid; d = 1536, V = 151936), in the benchmark's
     default chunk plan, against the oracle's full float64 dW; dH on every row."""
     w = WL.QWEN25_1P5B
     inp = WL.make_inputs(w)
