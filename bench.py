@@ -571,8 +571,15 @@ def main():
                     help="e4m3 operands for the H W^T GEMMs (row-wise quantized in the step)")
     ap.add_argument("--ref-given", action="store_true",
                     help="reference log-probs supplied; skip the reference GEMM half")
+    ap.add_argument("--seq-len", type=int, default=0,
+                    help="shorter sequences of the same workload (a smaller case of the same "
+                         "shapes for profiling; the workload is renamed <name>-T<len>)")
     args = ap.parse_args()
     w = WL.FULL.get(args.workload) or WL.SMALL[args.workload]
+    if args.seq_len > 0:
+        # same d, V and value recipe; padding bounds clipped to the new length
+        w = w.scaled("%s-T%d" % (w.name, args.seq_len), T=args.seq_len,
+                     pad_lo=min(w.pad_lo, args.seq_len), pad_hi=min(w.pad_hi, args.seq_len))
     if args.impl == "reference":
         run_reference(args, w)
     else:
