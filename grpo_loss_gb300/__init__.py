@@ -20,6 +20,9 @@ __all__ = ["GrpoError", "Problem", "advantages", "device_status", "loss_bwd", "l
            "quantize_e4m3_rows", "workspace_size", "GRPOLoss", "grpo_loss"]
 
 
+_CTRL_BYTES = 256  # control block at the start of every workspace (error word, counts)
+
+
 class GRPOLoss:
     """Owns the workspaces of one problem shape and runs the library calls.
 
@@ -50,6 +53,11 @@ class GRPOLoss:
         dev = torch.device(device)
         self.ws_fwd = torch.empty(fwd_b, dtype=torch.uint8, device=dev)
         self.ws_bwd = torch.empty(bwd_b, dtype=torch.uint8, device=dev)
+        # every call clears its workspace's control block (the device error
+        # word) first; clear both now, so check() before a backward has run
+        # does not read stale bytes from the allocator's cache
+        self.ws_fwd[:_CTRL_BYTES].zero_()
+        self.ws_bwd[:_CTRL_BYTES].zero_()
         N = num_seqs * seq_len
         self.adv = torch.empty(num_seqs, dtype=torch.float32, device=dev)
         self.logp_pol = torch.empty(N, dtype=torch.float32, device=dev)
