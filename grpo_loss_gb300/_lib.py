@@ -13,7 +13,9 @@ from typing import Optional
 
 import torch
 
-LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libgrpo_gb300.so")
+# The in-tree build; GRPO_GB300_LIB may name another build of the same library.
+LIB_PATH = os.environ.get("GRPO_GB300_LIB") or os.path.join(
+    os.path.dirname(os.path.abspath(__file__)), "libgrpo_gb300.so")
 
 GRPO_OK = 0
 STATUS_NAMES = {0: "GRPO_OK", 1: "GRPO_ERR_INVALID_ARG", 2: "GRPO_ERR_UNSUPPORTED",
