@@ -183,11 +183,20 @@ __device__ __forceinline__ Unit unit_decode(const GemmArgs& g, int nb, int u, in
     // dZ rows are chunk-local; a missing partner reads past the chunk (zeros)
     r.a_row = (r.valid ? r.jj : g.chunk_nb) * kBM;
   } else {
-    // MODE_DW: output tile (vocab rows mt*128.., hidden columns t*bn..)
-    const int p = u / g.n_nt;
+    // MODE_DW: output tile (vocab rows mt*128.., hidden columns t*bn..).
+    // Column tiles in groups of g.nt_group, as for dH: the resident units
+    // cover sms / nt_group vocab tiles x nt_group column tiles, trading
+    // re-reads of the dZ^T rows (once per group) against re-reads of H^T
+    // (once per wave); with all 16 column tiles side by side H^T was
+    // re-read from DRAM every wave (18.7 GB per Llama-head chunk, 15.9 GB
+    // grouped by 8).
+    const int per_grp = per_unit<PAIRED>(g.n_mt) * g.nt_group;
+    const int grp = u / per_grp;
+    const int rem = u - grp * per_grp;
+    const int p = rem / g.nt_group;
     r.jj = PAIRED ? 2 * p + rank : p;
     r.valid = r.jj < g.n_mt;
-    r.t0 = u - p * g.n_nt;
+    r.t0 = grp * g.nt_group + (rem - p * g.nt_group);
     r.t1 = r.t0 + 1;
     r.side = 0;
     r.vs = 0;

@@ -714,7 +714,7 @@ grpo_status loss_bwd_impl(const grpo_problem* problem, const void* H_pol, const 
   g.n_nt = P.n_nt;
   g.chunk_nb = P.chunk_nb;
   g.group_blocks = P.sms / 4 > 16 ? P.sms / 4 : 16;
-  // dH raster: at most 8 column tiles side by side (a divisor of n_nt)
+  // dH and dW rasters: at most 8 column tiles side by side (a divisor of n_nt)
   g.nt_group = 1;
   for (int q = 8; q >= 1; --q)
     if (P.n_nt % q == 0) {
