@@ -547,6 +547,24 @@ __global__ void __launch_bounds__(Warps<HALVES>::kThreads, 1)
         tc_fence_after();
         const uint32_t tbase = lane_addr + static_cast<uint32_t>(ab * kAccStride);
         const int64_t col_t = static_cast<int64_t>(t) * g.bn;
+        if (MODE == MODE_DZ && !CLUSTER && g.pf_group > 0 && u + unit_stride < n_units) {
+          // L2 prefetch of this CTA's next tile of W. When this tile's
+          // accumulator is full, the MMAs of the next tile have begun and the
+          // producer is only a few K blocks into it; the rest of its W rows
+          // would each be missed in L2 by the first CTA of the raster group to
+          // reach them, stalling that CTA's pipeline. The pf_group CTAs of
+          // the group split the 128-byte lines of the tile's rows by their
+          // block's rank in the group, so every line is requested once.
+          const int nt = unit_decode<MODE, CLUSTER>(g, nb, u + unit_stride, rank).t0;
+          const int64_t lines_per_row = g.pf_ld / 128;
+          const int64_t nlines = static_cast<int64_t>(g.bn) * lines_per_row;
+          const int64_t step = static_cast<int64_t>(g.pf_group) * Warps<HALVES>::kEpiThreads;
+          for (int64_t L = un.jj % g.pf_group + static_cast<int64_t>(g.pf_group) * (threadIdx.x - 64);
+               L < nlines; L += step) {
+            const int64_t v = static_cast<int64_t>(nt) * g.bn + L / lines_per_row;
+            if (v < g.V) prefetch_l2(g.pf_b + v * g.pf_ld + (L % lines_per_row) * 128);
+          }
+        }
 
         if (MODE == MODE_FWD) {
           float ts = 0.f;  // this tile's sum, relative to m2

@@ -755,6 +755,11 @@ grpo_status loss_bwd_impl(const grpo_problem* problem, const void* H_pol, const 
     gz.sb = s_W;
     // short tiles: two epilogue warps per row quadrant (no dZ^T staging)
     gz.epi_halves = (!P.dw && P.nk_d <= kDzSplitMaxKBlocks) ? 2 : 1;
+    // epilogue L2 prefetch of each CTA's next W tile, split among the blocks
+    // of a raster group (not for CTA pairs)
+    gz.pf_b = static_cast<const uint8_t*>(w);
+    gz.pf_ld = P.d * (P.e4m3 ? 1 : 2);
+    gz.pf_group = pair ? 0 : g.group_blocks;
     LAUNCH(K_BWD_DZ_GEMM, stream, launch_gemm(MODE_DZ, kind, mHp, mDzStore, mW, mDzTStore, gz, grid_dz, stream));
     GemmArgs gh = g;
     gh.bn = P.bn_dh;

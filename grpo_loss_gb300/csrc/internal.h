@@ -73,6 +73,11 @@ struct GemmArgs {
   const float* sa1;       // MODE_FWD: row scales of the reference rows
   const float* sb;        // row scales of B (the vocab rows of W)
   int epi_halves;         // MODE_FWD, MODE_DZ: 1 or 2 epilogue warps per row quadrant
+  // MODE_DZ: L2 prefetch of the B rows (W) of each CTA's next tile by the
+  // epilogue threads, shared among the pf_group CTAs of a raster group (0 = off)
+  const uint8_t* pf_b;    // W, row-major
+  int64_t pf_ld;          // bytes per W row
+  int pf_group;
 };
 
 // Profiling kinds (one per kernel the library launches).
