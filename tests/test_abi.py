@@ -76,6 +76,16 @@ def test_workspace_size_rejects_bad_problems_on_host(lib, field, value, expected
     assert lib.grpo_workspace_size(ctypes.byref(p), ctypes.byref(f), ctypes.byref(b)) == expected
 
 
+def test_chunk_plan_rejects_bad_problems_on_host(lib):
+    p = _problem(group_size=3)
+    r, n, b = ctypes.c_int64(0), ctypes.c_int32(0), ctypes.c_size_t(0)
+    assert lib.grpo_chunk_plan(ctypes.byref(p), ctypes.byref(r), ctypes.byref(n),
+                               ctypes.byref(b)) == 1
+    assert lib.grpo_chunk_plan(None, None, None, None) == 1
+    p = _problem(chunk_rows=-5)
+    assert lib.grpo_chunk_plan(ctypes.byref(p), None, None, None) == 1
+
+
 def test_null_problem_and_pointers_rejected(lib):
     assert lib.grpo_workspace_size(None, None, None) == 1
     assert lib.grpo_advantages(None, 8, 4, 1e-4, 1, None, None) == 1
