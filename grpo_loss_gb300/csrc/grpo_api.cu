@@ -321,7 +321,27 @@ grpo_status make_plan(const grpo_problem* p, Plan* pl) {
     if (nbmax < 1) nbmax = 1;
     // prefer a multiple of the blocks that make the dH tile count a multiple of the SMs
     const int m0 = sms / gcd_i(sms, P.n_nt);
-    if (nbmax >= m0) nbmax = nbmax / m0 * m0;
+    if (nbmax >= m0) {
+      nbmax = nbmax / m0 * m0;
+    } else {
+      // Fewer blocks fit than a whole number of waves needs (n_nt coprime
+      // with the SM count, as the 15 column tiles of d = 2880): take, from
+      // 3/4 of the budget up, the block count whose dH tiles fill their last
+      // wave best, ties to the larger. A dH tile runs over the whole vocab,
+      // so a ragged last wave idles SMs for the length of a tile (83 blocks
+      // x 15 tiles = 8.19 waves; 81 blocks = 7.99 waves).
+      int64_t best = nbmax;
+      double best_eff = -1.0;
+      for (int64_t b = nbmax; b >= 1 && 4 * b >= 3 * nbmax; --b) {
+        const double waves = static_cast<double>(b) * P.n_nt / sms;
+        const double eff = waves / ceil(waves);
+        if (eff > best_eff + 1e-9) {
+          best_eff = eff;
+          best = b;
+        }
+      }
+      nbmax = best;
+    }
     P.chunk_nb = static_cast<int>(nbmax);
   }
   if (P.chunk_nb > P.nblk_max) P.chunk_nb = P.nblk_max;

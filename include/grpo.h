@@ -126,9 +126,10 @@ grpo_status grpo_workspace_size(const grpo_problem *problem, size_t *fwd_bytes,
  * dZ (blocks * 128 rows * ldv columns * 2 bytes, ldv = V rounded up to a
  * multiple of 8) fits GRPO_DEFAULT_DZ_BUDGET_BYTES, rounded down to a
  * multiple of SMs / gcd(SMs, dH column tiles) blocks when that many fit, so
- * each chunk's dH GEMM fills whole waves of the device's SMs; otherwise it
- * is chunk_rows rounded up to a multiple of 128; never more than the
- * problem's blocks.
+ * each chunk's dH GEMM fills whole waves of the device's SMs; when fewer fit,
+ * the count between 3/4 of that largest one and the largest whose dH tiles
+ * fill their last wave best (ties to the larger). Otherwise it is chunk_rows
+ * rounded up to a multiple of 128; never more than the problem's blocks.
  *   chunk_rows      rows per chunk (a multiple of 128)
  *   n_chunks        chunks the backward launches (ceil of blocks / chunk)
  *   dz_chunk_bytes  bytes of the dZ chunk buffer in the backward workspace
