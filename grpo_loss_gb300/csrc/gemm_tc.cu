@@ -14,7 +14,8 @@
 //             domain) and the gather of the target logit. The logits never
 //             leave tensor memory.
 //   MODE_DZ   Z = H_pol W^T recomputed for one chunk of rows; the epilogue
-//             writes dZ = c * (softmax(z) - onehot(y)) as bf16.
+//             writes dZ = c * (softmax(z) - onehot(y)) as bf16, and at the
+//             start of each tile prefetches the CTA's next W tile into L2.
 //   MODE_DH   dH = dZ W for the same chunk (K = V), stored in H's dtype,
 //             with B = W^T [d, V] (K-major; transposed once per call, which
 //             measured faster than reading W MN-major).
