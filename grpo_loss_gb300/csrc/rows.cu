@@ -374,6 +374,103 @@ __global__ void k_transpose_w(const void* __restrict__ W, const float* __restric
   }
 }
 
+// bf16 W [V, d] -> Wt [d, ldwt] in 64 x 64 tiles with 16-byte accesses on
+// both sides (d and ldwt multiples of 8; W and Wt 16-byte aligned). A
+// thread moves 8 elements per access: rows of the tile are read as 8 chunks
+// of 16 bytes by 8 consecutive threads, and written back the same way as
+// rows of Wt. The tile is held as float with a 65-word row pitch, so the
+// row-wise writes and the column-wise reads of a warp (4 rows x 8 chunks)
+// fall in 32 different banks. Columns of Wt past V (up to ldwt) get zeros.
+constexpr int kTT = 64;  // tile edge of the vectorized transposes
+__global__ void __launch_bounds__(256) k_transpose_w_bf16(const __nv_bfloat16* __restrict__ W,
+                                                          int64_t V, int64_t d,
+                                                          __nv_bfloat16* __restrict__ Wt,
+                                                          int64_t ldwt) {
+  __shared__ float tile[kTT][kTT + 1];
+  const int64_t r0 = static_cast<int64_t>(blockIdx.x) * kTT;  // rows of W
+  const int64_t c0 = static_cast<int64_t>(blockIdx.y) * kTT;  // columns of W
+  const int i = threadIdx.x >> 3, j = threadIdx.x & 7;
+#pragma unroll
+  for (int p = 0; p < 2; ++p) {
+    const int rr = i + 32 * p;
+    const int64_t r = r0 + rr, c = c0 + 8 * j;
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (r < V && c < d) v = *reinterpret_cast<const uint4*>(W + r * d + c);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      tile[rr][8 * j + 2 * k] = __uint_as_float(w[k] << 16);
+      tile[rr][8 * j + 2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
+    }
+  }
+  __syncthreads();
+#pragma unroll
+  for (int p = 0; p < 2; ++p) {
+    const int cc = i + 32 * p;
+    const int64_t c = c0 + cc, r = r0 + 8 * j;
+    if (c < d && r < ldwt) {
+      uint32_t w[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const uint32_t lo = __float_as_uint(tile[8 * j + 2 * k][cc]) >> 16;
+        const uint32_t hi = __float_as_uint(tile[8 * j + 2 * k + 1][cc]) & 0xFFFF0000u;
+        w[k] = lo | hi;
+      }
+      *reinterpret_cast<uint4*>(Wt + c * ldwt + r) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+  }
+}
+
+// e4m3 W codes [V, d] with row scales -> bf16 Wt [d, ldwt], vectorized as
+// k_transpose_w_bf16 (8 codes per 8-byte load; d a multiple of 16). Each
+// element is decoded exactly, multiplied by its row's scale in float32 and
+// rounded to bf16 to nearest even, as the element-wise kernel does.
+__global__ void __launch_bounds__(256) k_transpose_w_e4m3(const uint8_t* __restrict__ W,
+                                                          const float* __restrict__ w_scale,
+                                                          int64_t V, int64_t d,
+                                                          __nv_bfloat16* __restrict__ Wt,
+                                                          int64_t ldwt) {
+  __shared__ float tile[kTT][kTT + 1];
+  const int64_t r0 = static_cast<int64_t>(blockIdx.x) * kTT;
+  const int64_t c0 = static_cast<int64_t>(blockIdx.y) * kTT;
+  const int i = threadIdx.x >> 3, j = threadIdx.x & 7;
+#pragma unroll
+  for (int p = 0; p < 2; ++p) {
+    const int rr = i + 32 * p;
+    const int64_t r = r0 + rr, c = c0 + 8 * j;
+    float f[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    if (r < V && c < d) {
+      const uint2 q = *reinterpret_cast<const uint2*>(W + r * d + c);
+      const float sc = w_scale[r];
+      const uint32_t b[2] = {q.x, q.y};
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        __nv_fp8_e4m3 v;
+        v.__x = static_cast<uint8_t>((b[k >> 2] >> (8 * (k & 3))) & 0xFFu);
+        f[k] = static_cast<float>(v) * sc;
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < 8; ++k) tile[rr][8 * j + k] = f[k];
+  }
+  __syncthreads();
+#pragma unroll
+  for (int p = 0; p < 2; ++p) {
+    const int cc = i + 32 * p;
+    const int64_t c = c0 + cc, r = r0 + 8 * j;
+    if (c < d && r < ldwt) {
+      uint32_t w[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const __nv_bfloat162 h =
+            __floats2bfloat162_rn(tile[8 * j + 2 * k][cc], tile[8 * j + 2 * k + 1][cc]);
+        w[k] = *reinterpret_cast<const uint32_t*>(&h);
+      }
+      *reinterpret_cast<uint4*>(Wt + c * ldwt + r) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+  }
+}
+
 // ----------------------------------------------------- compacted H^T
 // Ht[c][r] = bf16(H[src(r)][c]) for compacted rows r in [0, nblk_max * 128):
 // the row of block blk[r / 128] at offset r % 128, or 0 past the valid blocks
@@ -547,6 +644,23 @@ cudaError_t launch_bwd_coef(const uint8_t* mask, const int* cnt, const float* ad
 
 cudaError_t launch_transpose_w(const void* W, int w_type, const float* w_scale, int64_t V,
                                int64_t d, __nv_bfloat16* Wt, int64_t ldwt, cudaStream_t s) {
+  if (w_type == ELT_BF16 && d % 8 == 0 && ldwt % 8 == 0 &&
+      (reinterpret_cast<uintptr_t>(W) & 15) == 0 && (reinterpret_cast<uintptr_t>(Wt) & 15) == 0) {
+    // every column of Wt up to ldwt is written (zeros past V)
+    dim3 grid(static_cast<unsigned>((ldwt + kTT - 1) / kTT),
+              static_cast<unsigned>((d + kTT - 1) / kTT));
+    k_transpose_w_bf16<<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(W), V, d, Wt,
+                                            ldwt);
+    return cudaGetLastError();
+  }
+  if (w_type == ELT_E4M3 && d % 8 == 0 && ldwt % 8 == 0 &&
+      (reinterpret_cast<uintptr_t>(W) & 7) == 0 && (reinterpret_cast<uintptr_t>(Wt) & 15) == 0) {
+    dim3 grid(static_cast<unsigned>((ldwt + kTT - 1) / kTT),
+              static_cast<unsigned>((d + kTT - 1) / kTT));
+    k_transpose_w_e4m3<<<grid, 256, 0, s>>>(static_cast<const uint8_t*>(W), w_scale, V, d, Wt,
+                                            ldwt);
+    return cudaGetLastError();
+  }
   dim3 grid(static_cast<unsigned>((V + 31) / 32), static_cast<unsigned>((d + 31) / 32));
   dim3 block(32, 8);
   if (w_type == ELT_F32)
@@ -558,10 +672,67 @@ cudaError_t launch_transpose_w(const void* W, int w_type, const float* w_scale, 
   return cudaGetLastError();
 }
 
+// bf16 H -> compacted Ht, vectorized as k_transpose_w_bf16: compacted row r
+// of the tile comes from row blk[r / 128] * 128 + r % 128 of H, or is 0 past
+// the valid blocks or past N.
+__global__ void __launch_bounds__(256) k_transpose_h_bf16(const __nv_bfloat16* __restrict__ H,
+                                                          int64_t N, int64_t d,
+                                                          const int* __restrict__ blk,
+                                                          const int* nblk_dev,
+                                                          __nv_bfloat16* __restrict__ Ht,
+                                                          int64_t ldht) {
+  __shared__ float tile[kTT][kTT + 1];
+  const int nb = *nblk_dev;
+  const int64_t r0 = static_cast<int64_t>(blockIdx.x) * kTT;  // compacted rows
+  const int64_t c0 = static_cast<int64_t>(blockIdx.y) * kTT;  // hidden columns
+  const int i = threadIdx.x >> 3, j = threadIdx.x & 7;
+#pragma unroll
+  for (int p = 0; p < 2; ++p) {
+    const int rr = i + 32 * p;
+    const int64_t r = r0 + rr, c = c0 + 8 * j;
+    const int64_t jb = r / kBM;
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (jb < nb && c < d) {
+      const int64_t src = static_cast<int64_t>(blk[jb]) * kBM + (r - jb * kBM);
+      if (src < N) v = *reinterpret_cast<const uint4*>(H + src * d + c);
+    }
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      tile[rr][8 * j + 2 * k] = __uint_as_float(w[k] << 16);
+      tile[rr][8 * j + 2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
+    }
+  }
+  __syncthreads();
+#pragma unroll
+  for (int p = 0; p < 2; ++p) {
+    const int cc = i + 32 * p;
+    const int64_t c = c0 + cc, r = r0 + 8 * j;
+    if (c < d && r < ldht) {
+      uint32_t w[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const uint32_t lo = __float_as_uint(tile[8 * j + 2 * k][cc]) >> 16;
+        const uint32_t hi = __float_as_uint(tile[8 * j + 2 * k + 1][cc]) & 0xFFFF0000u;
+        w[k] = lo | hi;
+      }
+      *reinterpret_cast<uint4*>(Ht + c * ldht + r) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+  }
+}
+
 cudaError_t launch_transpose_h_compact(const void* H, int h_type, const float* h_scale,
                                        int64_t N, int64_t d, const int* blk, const int* nblk_dev,
                                        int nblk_max, __nv_bfloat16* Ht, int64_t ldht,
                                        cudaStream_t s) {
+  if (h_type == ELT_BF16 && d % 8 == 0 && ldht % 8 == 0 &&
+      (reinterpret_cast<uintptr_t>(H) & 15) == 0 && (reinterpret_cast<uintptr_t>(Ht) & 15) == 0) {
+    dim3 grid(static_cast<unsigned>((static_cast<int64_t>(nblk_max) * kBM + kTT - 1) / kTT),
+              static_cast<unsigned>((d + kTT - 1) / kTT));
+    k_transpose_h_bf16<<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(H), N, d, blk,
+                                            nblk_dev, Ht, ldht);
+    return cudaGetLastError();
+  }
   dim3 grid(static_cast<unsigned>(nblk_max * (kBM / 32)), static_cast<unsigned>((d + 31) / 32));
   dim3 block(32, 8);
   if (h_type == ELT_E4M3)
